@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the partial-sum reduction on GB300.
+
+One step = one ar_reduce call over one batch of the workload (every step of
+the hot path: load R partials, round each through the wire type, fold in
+float, cast back, store to every destination).  Default workload: prefill,
+R=2 f32[2048,4096], bf16 wire, 2 destinations (128 MiB moved per call).
+
+Prints ONE JSON line (rank 0).  Multi-GPU: launch under torchrun; every rank
+runs the same independent reduction on its own GPU (weak scaling, no
+collective on the data path); timing is the max over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (% of roofline) prefill-size; µs/call decode-size"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ar_vec_kernel_prefill_traffic.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", f) for f in ("ar_kernels.cuh", "ar.cu")]
+
+
+# ---- distributed plumbing (also exercised by the CPU tests with gloo) -------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank moved bytes_per_step * steps bytes;
+    the job took as long as its slowest rank."""
+    return world * bytes_per_step * steps / max_seconds / 1e9
+
+
+# ---- measured peaks, clocks, traffic -----------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def sources_digest() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when it
+    is missing, covers another workload, or the kernel sources changed since
+    the counters were taken."""
+    try:
+        fields = {}
+        with open(TRAFFIC_SUMMARY) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("workload") != workload or fields.get("source_digest") != sources_digest():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                ts = dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append({"t": ts, "sm": float(parts[1]), "max": float(parts[2]),
+                             "reasons": [n for n, v in zip(self.REASONS, parts[5:]) if v == "Active"]})
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        inside = [r for r in rows if t0 <= r["t"] <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside, window = rows, "sustained pre-run and timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        reasons = sorted({x for r in inside for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["max"] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+    except Exception:  # pragma: no cover - older torch
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ---- the oracle as CPU baseline ------------------------------------------------
+
+def oracle_rate(srcs, w, seconds: float):
+    """Time the oracle (single thread, as it stands) on a prefix sample of the
+    workload sized to take about ``seconds``; returns (GB/s, sample text)."""
+    import oracle
+    probe = min(w.nelem, 1 << 16)
+    t = time.perf_counter()
+    oracle.reduce([s[:probe] for s in srcs], w.n_dsts, w.dst, w.wire)
+    per_elem = max((time.perf_counter() - t) / probe, 1e-9)
+    n = int(min(w.nelem, max(probe, seconds / per_elem)))
+    reps = max(1, int(seconds / (per_elem * n)))
+    sample = [s[:n] for s in srcs]
+    out = None
+    t = time.perf_counter()
+    for _ in range(reps):
+        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
+    el = time.perf_counter() - t
+    moved = (w.R + w.n_dsts) * n * w.elem_bytes * reps
+    return moved / el / 1e9, el, f"first {n} of {w.nelem} elements of each rank, {reps} pass(es), {el:.1f} s"
+
+
+# ---- our arm -----------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import tensor_partial_sum_gb300 as tps
+    from tensor_partial_sum_gb300 import build as lib_build
+    from tensor_partial_sum_gb300 import workloads as W
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist_init(world, "nccl")
+    if lib_build.stale():
+        if rank == 0:
+            lib_build.build()
+        barrier()
+    w = W.WORKLOADS[args.workload]
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dst]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 129 * 1000 * 1000) or 129 * 1000 * 1000
+    sampler = ClockSampler(gpu_id_for(local_rank))
+
+    srcs_np = W.generate(w)
+
+    def dev_tensor(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.to(dev).view(tdt)
+
+    # rotating buffer sets: each step's inputs were last touched sets-1 steps ago
+    nsets = 1 if w.bytes_per_call >= 3 * l2 else math.ceil(3 * l2 / w.bytes_per_call)
+    base_src = [dev_tensor(a) for a in srcs_np]
+    sets = []
+    for k in range(nsets):
+        s = base_src if k == 0 else [b.clone() for b in base_src]
+        d = [torch.empty(w.nelem, dtype=tdt, device=dev) for _ in range(w.n_dsts)]
+        sets.append((s, d))
+    stream = torch.cuda.Stream(dev)
+    tps.ar_init(w.R, w.nelem)
+
+    def step(i):
+        s, d = sets[i % nsets]
+        tps.ar_reduce(s, d, nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+    variant = {v: k for k, v in tps.ar.VARIANTS.items()}[tps.ar_query("last_variant")]
+
+    # graph of G steps with an event pair around every launch
+    G = max(1, min(args.steps, nsets * max(1, math.ceil(64 / nsets))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+    replays, rem = divmod(args.steps, G)
+
+    sampler.start()
+    with torch.cuda.stream(stream):  # sustained pre-run so clocks are sampled under load
+        t_end = time.perf_counter() + args.sustain
+        while time.perf_counter() < t_end:
+            graph.replay()
+            torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = dt.datetime.now()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        for i in range(rem):
+            step(i)
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = dt.datetime.now()
+    barrier()
+    clocks = ClockSampler.summarize(sampler.stop(), t0, t1)
+    elapsed = start.elapsed_time(end) / 1e3
+    max_elapsed = max_over_ranks(elapsed, dev)
+    value = aggregate_gbs(w.bytes_per_call, args.steps, world, max_elapsed)
+    kernel_s = None
+    if replays > 0:
+        kernel_s = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    if not kernel_s:
+        kernel_s = elapsed / args.steps
+    peak, peak_src = hbm_peak()
+    achieved = w.bytes_per_call / kernel_s / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_elapsed * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}", "bytes_per_step": w.bytes_per_call,
+                   "variant": variant, "parallelism": f"{world} independent replica(s), no collective",
+                   "l2": f"{nsets} rotating buffer sets ({nsets * w.bytes_per_call / 2**20:.0f} MiB) cycled, "
+                         f"L2 {l2 / 2**20:.0f} MiB: each step's inputs were last touched {nsets - 1} steps earlier"
+                         if nsets > 1 else f"inputs {w.bytes_per_call / 2**20:.0f} MiB > 3x L2",
+                   "timing": f"CUDA graph of {G} launches replayed {replays}x (+{rem} eager), CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic_per_launch(w.name),
+                     "peak_source": peak_src, "kernel_us": round(kernel_s * 1e6, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    # end to end through the host entry point: pinned host partials in, results out
+    if args.e2e_steps > 0:
+        h_srcs = [torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory() for a in srcs_np]
+        h_dsts = [torch.empty(w.nelem, dtype=h_srcs[0].dtype).pin_memory() for _ in range(w.n_dsts)]
+        d_srcs, d_dsts = sets[0]
+
+        def e2e_step():
+            tps.ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, nelem=w.nelem, dst_dtype=w.dst,
+                               wire_dtype=w.wire, stream=stream)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_el = max_over_ranks(a.elapsed_time(b) / 1e3, dev)
+        result["e2e"] = {"value": round(aggregate_gbs(w.bytes_per_call, args.e2e_steps, world, e_el), 2),
+                         "unit": UNIT, "h2d_bytes_per_step": w.R * w.nelem * w.elem_bytes,
+                         "d2h_bytes_per_step": w.n_dsts * w.nelem * w.elem_bytes, "steps": args.e2e_steps,
+                         "call": "ar_reduce_host (pinned host buffers)"}
+
+    del sets, base_src
+    torch.cuda.empty_cache()
+    if args.decode:
+        result["decode"] = bench_decode(dev, stream)
+
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        v, el, sample = oracle_rate(srcs_np, w, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": sample}
+    tps.ar_free()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def bench_decode(dev, stream):
+    """Decode-sized calls: R=4 f32[1,4099], f16 wire, 4 destinations, 10000
+    calls with their own buffers and per-call seeds, captured in one CUDA
+    graph; microseconds per call = graph replay time / calls."""
+    import numpy as np
+    import torch
+
+    import tensor_partial_sum_gb300 as tps
+    from tensor_partial_sum_gb300 import workloads as W
+
+    w = W.WORKLOADS["decode"]
+    row = (w.nelem + 3) // 4 * 4  # pad rows to 16 bytes so every buffer is aligned
+    buf = torch.zeros((w.calls, w.R + w.n_dsts, row), dtype=torch.float32, device=dev)
+    host = np.zeros((w.calls, w.R, w.nelem), dtype=np.float32)
+    for k in range(w.calls):
+        host[k] = np.stack(W.generate(w, call=k))
+    buf[:, :w.R, :w.nelem].copy_(torch.from_numpy(host))
+    del host
+    tps.ar_init(w.R, w.nelem)
+    ptr = buf.data_ptr()
+    stride_call, stride_buf = buf.stride(0) * 4, buf.stride(1) * 4
+    calls = [([ptr + k * stride_call + r * stride_buf for r in range(w.R)],
+              [ptr + k * stride_call + (w.R + d) * stride_buf for d in range(w.n_dsts)]) for k in range(w.calls)]
+
+    def one(k):
+        s, d = calls[k]
+        tps.ar_reduce(s, d, nelem=w.nelem, dst_dtype="f32", wire_dtype=w.wire, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for k in range(min(100, w.calls)):
+            one(k)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(w.calls):
+            one(k)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    with torch.cuda.stream(stream):
+        graph.replay()
+        for _ in range(5):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b) * 1e3 / w.calls)
+        a.record(stream)
+        for k in range(w.calls):
+            one(k)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    eager = a.elapsed_time(b) * 1e3 / w.calls
+    variant = {v: k for k, v in tps.ar.VARIANTS.items()}[tps.ar_query("last_variant")]
+    del graph, buf
+    return {"us_per_call": round(statistics.median(times), 3), "unit": "µs/call",
+            "target_us": 5.0, "workload": f"{w.name}: {w.describe()}", "variant": variant,
+            "timing": f"one CUDA graph of {w.calls} ar_reduce nodes, median of 5 replays",
+            "us_per_call_eager_stream": round(eager, 3),
+            "bytes_per_call": w.bytes_per_call}
+
+
+# ---- reference arm: the oracle on the host cores ------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from tensor_partial_sum_gb300 import workloads as W
+    import oracle
+
+    w = W.WORKLOADS[args.workload]
+    srcs = W.generate(w)
+    probe = min(w.nelem, 1 << 16)
+    t = time.perf_counter()
+    oracle.reduce([s[:probe] for s in srcs], w.n_dsts, w.dst, w.wire)
+    per_elem = max((time.perf_counter() - t) / probe, 1e-9)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    n = int(min(w.nelem, max(256, budget / per_elem)))
+    sample = [s[:n] for s in srcs]
+    out = None
+    for _ in range(args.warmup):
+        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
+    el = time.perf_counter() - t
+    value = (w.R + w.n_dsts) * n * w.elem_bytes * args.steps / el / 1e9
+    text = f"first {n} of {w.nelem} elements of each rank per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}", "bytes_per_step": (w.R + w.n_dsts) * n * w.elem_bytes,
+                   "parallelism": "oracle on rank 0 only"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": text},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="prefill")
+    p.add_argument("--e2e-steps", type=int, default=100)
+    p.add_argument("--sustain", type=float, default=1.0, help="seconds of untimed load before timing")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--ref-seconds", type=float, default=60.0)
+    p.add_argument("--no-decode", dest="decode", action="store_false")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.steps < 1:
+        p.error("--steps must be at least 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * ar.h -- C ABI of the GB300 partial-sum reduction (libtps_ar.so).
+ *
+ * The operation is the reduction step of a tensor-parallel AllReduce, done
+ * on one GPU: R partial tensors ("ranks") of one activation, each in its own
+ * device allocation, are each rounded through a narrower wire type, summed
+ * in float in ascending rank order, and the sum is cast back to the tensor
+ * type and written to every destination buffer:
+ *
+ *   for every element i:
+ *     acc = float(wire(src[0][i]))
+ *     acc = acc + float(wire(src[r][i]))        r = 1 .. R-1, in this order
+ *     dst[d][i] = T_dst(acc)                     d = 0 .. n_dsts-1
+ *
+ * wire(x) and T_dst(x) round to nearest, ties to even, keep subnormals and
+ * overflow to infinity; float(x) is exact; the adds are float adds rounded
+ * to nearest.  The result is bit-for-bit the same for every variant, grid
+ * size and alignment (NaN payloads aside).
+ *
+ * Where this comes from:
+ *   - ggml-cuda allreduce.cu (toy 0.8.0 vendored ggml), ggml_cuda_ar_kernel,
+ *     phases 1 and 3, and ggml_cuda_ar_add_kernel: both operands are rounded
+ *     through the wire type, widened to float, added in float and the sum is
+ *     cast back to the tensor type, so that every rank computes identical
+ *     bits; ggml_cuda_ar_allreduce picks the wire type (bf16 for f32 tensors)
+ *     and the strategy by tensor size.
+ *   - ggml-hexagon htp/allreduce-ops.c (char-fork/llama.cpp),
+ *     DEFINE_ALLREDUCE_THREAD_DMA_1D: the ranks are folded left to right and
+ *     the result is written to each of n_dsts destinations; validate_allreduce
+ *     and op_allreduce return status codes instead of asserting.
+ *   - The float accumulator for R > 2, the start from rank 0's operand (not
+ *     from zero) and the rounding rules are this library's readings where the
+ *     pages are silent.
+ *
+ * Conventions for every call below:
+ *   - Device pointers are plain CUDA device addresses on the device that was
+ *     current at ar_init; host pointers are ordinary (ideally pinned) host
+ *     memory.  The caller owns every buffer and the stream; the library
+ *     keeps no pointer after a call returns and allocates nothing per call.
+ *   - Calls that take a stream only enqueue work on it and return; results
+ *     are ready when the stream reaches that point.  No call synchronizes,
+ *     so ar_reduce and ar_reduce_variant can be captured in a CUDA graph.
+ *   - On any status other than AR_OK nothing has been enqueued or written,
+ *     except AR_ERR_CUDA from a launch, after which the stream's state is
+ *     whatever CUDA reports.
+ *   - All calls are thread-safe; they share one process-wide context.
+ */
+#ifndef TPS_AR_H
+#define TPS_AR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (identical to its own typedef). */
+typedef struct CUstream_st *cudaStream_t;
+
+/* Element types.  Sources and destinations hold T_dst; T_wire is the type
+ * every operand is rounded through before the float sum. */
+typedef enum { AR_F32 = 0, AR_F16 = 1, AR_BF16 = 2 } ar_dtype;
+
+typedef enum {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = 1,     /* bad count, NULL pointer, wrong device, ... */
+    AR_ERR_UNSUPPORTED = 2,     /* unknown dtype, or the GPU cannot run the kernels */
+    AR_ERR_TOO_LARGE = 3,       /* nelem > max_elems given to ar_init */
+    AR_ERR_NOT_INITIALIZED = 4, /* ar_init has not succeeded */
+    AR_ERR_OVERLAP = 5,         /* a destination partly overlaps another buffer */
+    AR_ERR_CUDA = 6             /* a CUDA call failed */
+} ar_status;
+
+/* Limits: at most 16 ranks and 16 destinations per call (the pages cap
+ * their rank arrays at compile-time maxima of this order:
+ * GGML_CUDA_MAX_DEVICES in allreduce.cu, HTP_ALLREDUCE_MAX_RANKS in
+ * allreduce-ops.c). */
+#define AR_MAX_RANKS 16
+#define AR_MAX_DSTS 16
+
+/* Kernel variants.  AUTO picks LATENCY or BANDWIDTH by the call's byte
+ * count (and SCALAR when a pointer is not 16-byte aligned).  Every variant
+ * computes the same bits. */
+typedef enum {
+    AR_VARIANT_AUTO = 0,
+    AR_VARIANT_NAIVE = 1,     /* one element per thread, grid-stride: a cross-check */
+    AR_VARIANT_LATENCY = 2,   /* one 16-byte vector per thread, one small launch */
+    AR_VARIANT_BANDWIDTH = 3, /* persistent grid, several vectors per thread */
+    AR_VARIANT_SCALAR = 4     /* element-wise path used for unaligned pointers */
+} ar_variant;
+
+/*
+ * ar_init -- create the process-wide context on the current CUDA device.
+ *   R          number of ranks (partials) every ar_reduce call sums, 1..16.
+ *   max_elems  largest nelem any later call may pass (>= 1).
+ * Reads the environment once: AR_VARIANT (auto|naive|latency|bandwidth|
+ * scalar), AR_LATENCY_MAX_BYTES (size switch, bytes of sources plus
+ * destinations), AR_LOG=1 (one line per init to stderr).
+ * Calling it again replaces the context.  Returns AR_OK, AR_ERR_INVALID_ARG,
+ * AR_ERR_UNSUPPORTED (the device is not sm_103) or AR_ERR_CUDA (no device).
+ */
+int ar_init(int R, size_t max_elems);
+
+/*
+ * ar_reduce -- enqueue one reduction on `stream`.
+ *   srcs       host array of R device pointers, each to nelem elements of
+ *              dst_dtype (contiguous); read only.
+ *   dsts       host array of n_dsts device pointers, each to nelem elements
+ *              of dst_dtype; all receive the same bits.  A destination may
+ *              be exactly one of the sources (in-place reduction) but may
+ *              not partly overlap any source or other destination.
+ *   n_dsts     1..16.
+ *   nelem      elements per buffer, <= max_elems; 0 is a no-op (AR_OK).
+ *   dst_dtype  ar_dtype of sources and destinations.
+ *   wire_dtype ar_dtype every operand is rounded through (any of the three).
+ *   stream     CUDA stream of the init device (0 = legacy default stream).
+ * Any element-aligned pointer works; 16-byte-aligned pointers take the
+ * vector paths.  Returns an ar_status.
+ */
+int ar_reduce(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem,
+              int dst_dtype, int wire_dtype, cudaStream_t stream);
+
+/* ar_free -- drop the context.  Safe to call when not initialized. */
+void ar_free(void);
+
+/* Static English text for a status code (never NULL). */
+const char *ar_status_string(int status);
+
+/*
+ * ar_check_args -- the host-side validation ar_reduce runs before any CUDA
+ * call, on explicit R and max_elems instead of the context's.  Makes no CUDA
+ * call and touches no device memory, so it runs without a GPU.
+ */
+int ar_check_args(int R, const void *const *srcs, void *const *dsts, int n_dsts,
+                  size_t nelem, size_t max_elems, int dst_dtype, int wire_dtype);
+
+/*
+ * ar_reduce_variant -- ar_reduce with the kernel variant forced.
+ *   variant     an ar_variant; AUTO behaves exactly like ar_reduce.
+ *   grid_blocks CTAs to launch for BANDWIDTH/NAIVE/SCALAR (0 = the library's
+ *               choice); ignored by LATENCY, whose grid covers the tensor.
+ * The result bits do not depend on either argument.  A vector variant asked
+ * for with unaligned pointers returns AR_ERR_INVALID_ARG.
+ */
+int ar_reduce_variant(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem,
+                      int dst_dtype, int wire_dtype, int variant, int grid_blocks,
+                      cudaStream_t stream);
+
+/* Keys for ar_query / ar_set_option. */
+typedef enum {
+    AR_Q_RANKS = 0,             /* R fixed at ar_init (query only) */
+    AR_Q_MAX_ELEMS = 1,         /* max_elems (query only) */
+    AR_Q_DEVICE = 2,            /* CUDA device ordinal (query only) */
+    AR_Q_SM_COUNT = 3,          /* SMs on that device (query only) */
+    AR_Q_LATENCY_MAX_BYTES = 4, /* AUTO uses LATENCY below this many bytes */
+    AR_Q_FORCED_VARIANT = 5,    /* variant AUTO resolves to when nonzero */
+    AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only) */
+    AR_Q_FAULT_INJECT = 7,      /* nonzero: the next launches fail with AR_ERR_CUDA
+                                   before anything is enqueued (host-side test hook) */
+    AR_Q_BW_BLOCKS_PER_SM = 8   /* resident CTAs per SM of the BANDWIDTH grid (0 = occupancy) */
+} ar_key;
+
+/* Read one context value into *value.  AR_ERR_NOT_INITIALIZED before init. */
+int ar_query(int key, int64_t *value);
+
+/* Change one settable context value.  Not to be called while a stream
+ * capture that uses the library is in progress. */
+int ar_set_option(int key, int64_t value);
+
+/*
+ * ar_reduce_host -- the same reduction for callers whose partials live in
+ * host memory: copies each host source into the caller's device staging
+ * buffer, reduces into the caller's device destination buffers, and copies
+ * every destination back to its host buffer, all enqueued on `stream`.
+ *   h_srcs, h_dsts  R and n_dsts host pointers (pinned memory makes the
+ *                   copies asynchronous; pageable memory also works).
+ *   d_srcs, d_dsts  R and n_dsts device buffers of nelem elements each.
+ * Everything else as for ar_reduce.  The host results are valid once the
+ * stream has reached the end of this call.
+ */
+int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem,
+                   int dst_dtype, int wire_dtype, void *const *d_srcs, void *const *d_dsts,
+                   cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPS_AR_H */

@@ -1,0 +1,185 @@
+"""ctypes binding of libtps_ar.so, one Python function per C entry point.
+
+Argument marshalling only: tensors become device pointers, Python lists
+become pointer arrays, torch streams become ``cudaStream_t`` handles, and a
+non-zero status becomes an ``ARError``.  Every step of the reduction runs in
+the library's CUDA kernels; there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libtps_ar.so")
+
+AR_F32, AR_F16, AR_BF16 = 0, 1, 2
+DTYPE_CODES = {"f32": AR_F32, "f16": AR_F16, "bf16": AR_BF16}
+
+AR_OK = 0
+STATUS_NAMES = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3: "AR_ERR_TOO_LARGE",
+                4: "AR_ERR_NOT_INITIALIZED", 5: "AR_ERR_OVERLAP", 6: "AR_ERR_CUDA"}
+VARIANTS = {"auto": 0, "naive": 1, "latency": 2, "bandwidth": 3, "scalar": 4}
+KEYS = {"ranks": 0, "max_elems": 1, "device": 2, "sm_count": 3, "latency_max_bytes": 4,
+        "forced_variant": 5, "last_variant": 6, "fault_inject": 7, "bw_blocks_per_sm": 8}
+
+_lib = None
+
+
+class ARError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {STATUS_NAMES.get(status, status)} ({ar_status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built: run `python -m tensor_partial_sum_gb300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, sz, i, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        L.ar_init.argtypes = [i, sz]
+        L.ar_init.restype = i
+        L.ar_reduce.argtypes = [pp, pp, i, sz, i, i, vp]
+        L.ar_reduce.restype = i
+        L.ar_free.argtypes = []
+        L.ar_free.restype = None
+        L.ar_status_string.argtypes = [i]
+        L.ar_status_string.restype = ctypes.c_char_p
+        L.ar_check_args.argtypes = [i, pp, pp, i, sz, sz, i, i]
+        L.ar_check_args.restype = i
+        L.ar_reduce_variant.argtypes = [pp, pp, i, sz, i, i, i, i, vp]
+        L.ar_reduce_variant.restype = i
+        L.ar_query.argtypes = [i, ctypes.POINTER(i64)]
+        L.ar_query.restype = i
+        L.ar_set_option.argtypes = [i, i64]
+        L.ar_set_option.restype = i
+        L.ar_reduce_host.argtypes = [pp, pp, i, sz, i, i, pp, pp, vp]
+        L.ar_reduce_host.restype = i
+        _lib = L
+    return _lib
+
+
+# ---- marshalling helpers -------------------------------------------------
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):  # numpy array (host buffers)
+        return x.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(x).__name__}")
+
+
+AR_MAX_RANKS = 16
+
+
+def _ptrs(xs):
+    """Pointer array padded with NULLs to at least AR_MAX_RANKS entries, so
+    a list shorter than the context's R is rejected (NULL source) instead of
+    being read past its end."""
+    if xs is None:
+        return None
+    ptrs = [_ptr(x) for x in xs]
+    ptrs += [None] * max(0, AR_MAX_RANKS - len(ptrs))
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def _dtype_code(d) -> int:
+    if isinstance(d, int):
+        return d
+    if isinstance(d, str):
+        return DTYPE_CODES[d]
+    import torch
+    return {torch.float32: AR_F32, torch.float16: AR_F16, torch.bfloat16: AR_BF16}[d]
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def _infer(srcs, nelem, dst_dtype):
+    t = srcs[0] if srcs else None
+    if nelem is None:
+        nelem = t.numel()
+    if dst_dtype is None:
+        dst_dtype = t.dtype
+    return nelem, _dtype_code(dst_dtype)
+
+
+def _check(status: int, call: str) -> int:
+    if status != AR_OK:
+        raise ARError(status, call)
+    return status
+
+
+# ---- entry points ----------------------------------------------------------
+
+def ar_status_string(status: int) -> str:
+    return lib().ar_status_string(status).decode()
+
+
+def ar_init(R: int, max_elems: int) -> None:
+    _check(lib().ar_init(R, max_elems), "ar_init")
+
+
+def ar_free() -> None:
+    lib().ar_free()
+
+
+def ar_reduce(srcs, dsts, nelem=None, dst_dtype=None, wire_dtype="bf16", stream=None) -> None:
+    """Enqueue one reduction of ``srcs`` (R tensors or device pointers) into
+    every tensor of ``dsts``.  ``nelem``/``dst_dtype`` default to the first
+    source tensor's; ``stream`` defaults to torch's current stream."""
+    nelem, dcode = _infer(srcs, nelem, dst_dtype)
+    _check(lib().ar_reduce(_ptrs(srcs), _ptrs(dsts), len(dsts), nelem, dcode, _dtype_code(wire_dtype),
+                           _stream(stream)), "ar_reduce")
+
+
+def ar_reduce_variant(srcs, dsts, variant="auto", grid_blocks=0, nelem=None, dst_dtype=None,
+                      wire_dtype="bf16", stream=None) -> None:
+    nelem, dcode = _infer(srcs, nelem, dst_dtype)
+    v = VARIANTS[variant] if isinstance(variant, str) else variant
+    _check(lib().ar_reduce_variant(_ptrs(srcs), _ptrs(dsts), len(dsts), nelem, dcode, _dtype_code(wire_dtype),
+                                   v, grid_blocks, _stream(stream)), "ar_reduce_variant")
+
+
+def ar_check_args(R, srcs, dsts, n_dsts, nelem, max_elems, dst_dtype, wire_dtype) -> int:
+    """Host-only validation; returns the status code (does not raise)."""
+    return lib().ar_check_args(R, _ptrs(srcs), _ptrs(dsts), n_dsts, nelem, max_elems,
+                               _dtype_code(dst_dtype), _dtype_code(wire_dtype))
+
+
+def ar_query(key) -> int:
+    k = KEYS[key] if isinstance(key, str) else key
+    v = ctypes.c_int64(0)
+    _check(lib().ar_query(k, ctypes.byref(v)), "ar_query")
+    return v.value
+
+
+def ar_set_option(key, value: int) -> None:
+    k = KEYS[key] if isinstance(key, str) else key
+    _check(lib().ar_set_option(k, value), "ar_set_option")
+
+
+def ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, nelem=None, dst_dtype=None, wire_dtype="bf16",
+                   stream=None) -> None:
+    """Host partials in, host results out, through the caller's device
+    staging buffers; everything is enqueued on ``stream``."""
+    nelem, dcode = _infer(d_srcs, nelem, dst_dtype)
+    _check(lib().ar_reduce_host(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode, _dtype_code(wire_dtype),
+                                _ptrs(d_srcs), _ptrs(d_dsts), _stream(stream)), "ar_reduce_host")

@@ -1,0 +1,416 @@
+// C ABI of the partial-sum reduction: context, argument checks, variant
+// dispatch and launches.  The operation, its arguments and its error
+// behaviour are specified in include/ar.h.
+//
+// Structure follows the hook trio of the pages (init / allreduce / free in
+// ggml-cuda allreduce.cu: ggml_cuda_ar_pipeline_init, ggml_cuda_ar_allreduce,
+// ggml_cuda_ar_pipeline_free) without the transport: on one GPU the R
+// partials are plain device buffers, so a call is one kernel launch on the
+// caller's stream.  ggml_cuda_ar_allreduce chooses its strategy by byte
+// count; here the choice is between a one-shot latency launch and a
+// persistent bandwidth grid.  Status codes instead of asserts follow
+// validate_allreduce / op_allreduce in ggml-hexagon htp/allreduce-ops.c.
+#include "ar.h"
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ar_kernels.cuh"
+
+using tps::ArParams;
+
+namespace {
+
+constexpr int kLatencyThreads = 128;
+constexpr int kBandwidthThreads = 256;
+constexpr int kScalarThreads = 256;
+constexpr int64_t kDefaultLatencyMaxBytes = 4ll << 20;
+
+struct Context {
+    bool ready = false;
+    int R = 0;
+    size_t max_elems = 0;
+    int device = -1;
+    int sm_count = 0;
+    int64_t latency_max_bytes = kDefaultLatencyMaxBytes;
+    int forced_variant = AR_VARIANT_AUTO;
+    int last_variant = AR_VARIANT_AUTO;
+    int fault_inject = 0;
+    int bw_blocks_per_sm = 0;
+};
+
+std::mutex g_mu;
+Context g_ctx;
+
+size_t elem_bytes(int dtype) {
+    switch (dtype) {
+        case AR_F32: return 4;
+        case AR_F16: return 2;
+        case AR_BF16: return 2;
+        default: return 0;
+    }
+}
+
+bool ranges_overlap(uintptr_t a, uintptr_t b, size_t bytes) { return a < b + bytes && b < a + bytes; }
+
+// ---- kernel tables, indexed [dst dtype][wire dtype] ------------------------
+using KernelFn = void (*)(ArParams);
+
+template <int Td, int Tw>
+struct KernelSet {
+    static constexpr int kU = (Td == tps::kF32) ? 4 : 2;  // 64 or 32 bytes per thread per rank
+    static constexpr KernelFn latency[2] = {tps::ar_vec_kernel<Td, Tw, 1, false>,
+                                            tps::ar_vec_kernel<Td, Tw, 1, true>};
+    static constexpr KernelFn bandwidth[2] = {tps::ar_vec_kernel<Td, Tw, kU, false>,
+                                              tps::ar_vec_kernel<Td, Tw, kU, true>};
+    static constexpr KernelFn scalar[2] = {tps::ar_scalar_kernel<Td, Tw, false>,
+                                           tps::ar_scalar_kernel<Td, Tw, true>};
+    static constexpr KernelFn naive = tps::ar_naive_kernel<Td, Tw>;
+};
+
+struct Kernels {
+    KernelFn latency[2];
+    KernelFn bandwidth[2];
+    KernelFn scalar[2];
+    KernelFn naive;
+    int bandwidth_vecs_per_thread;
+};
+
+template <int Td, int Tw>
+Kernels make_kernels() {
+    using S = KernelSet<Td, Tw>;
+    return Kernels{{S::latency[0], S::latency[1]},
+                   {S::bandwidth[0], S::bandwidth[1]},
+                   {S::scalar[0], S::scalar[1]},
+                   S::naive,
+                   S::kU};
+}
+
+const Kernels &kernels_for(int dst, int wire) {
+    static const Kernels table[3][3] = {
+        {make_kernels<tps::kF32, tps::kF32>(), make_kernels<tps::kF32, tps::kF16>(),
+         make_kernels<tps::kF32, tps::kBF16>()},
+        {make_kernels<tps::kF16, tps::kF32>(), make_kernels<tps::kF16, tps::kF16>(),
+         make_kernels<tps::kF16, tps::kBF16>()},
+        {make_kernels<tps::kBF16, tps::kF32>(), make_kernels<tps::kBF16, tps::kF16>(),
+         make_kernels<tps::kBF16, tps::kBF16>()},
+    };
+    return table[dst][wire];
+}
+
+// Resident CTAs per SM of a kernel (queried once per kernel, then cached).
+struct OccEntry {
+    KernelFn fn;
+    int blocks;
+};
+OccEntry g_occ[64];
+int g_occ_n = 0;
+
+int blocks_per_sm(KernelFn fn, int threads) {
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].fn == fn) return g_occ[i].blocks;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reinterpret_cast<const void *>(fn), threads, 0) !=
+            cudaSuccess ||
+        b < 1)
+        b = 1;
+    if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{fn, b};
+    return b;
+}
+
+int parse_variant(const char *s) {
+    if (!s || !*s || !strcmp(s, "auto")) return AR_VARIANT_AUTO;
+    if (!strcmp(s, "naive")) return AR_VARIANT_NAIVE;
+    if (!strcmp(s, "latency")) return AR_VARIANT_LATENCY;
+    if (!strcmp(s, "bandwidth")) return AR_VARIANT_BANDWIDTH;
+    if (!strcmp(s, "scalar")) return AR_VARIANT_SCALAR;
+    return -1;
+}
+
+const char *variant_name(int v) {
+    switch (v) {
+        case AR_VARIANT_NAIVE: return "naive";
+        case AR_VARIANT_LATENCY: return "latency";
+        case AR_VARIANT_BANDWIDTH: return "bandwidth";
+        case AR_VARIANT_SCALAR: return "scalar";
+        default: return "auto";
+    }
+}
+
+int grid_cap(long long want, long long cap) {
+    if (want < 1) want = 1;
+    if (want > cap) want = cap;
+    return static_cast<int>(want);
+}
+
+// Launch one reduction; the caller holds g_mu and has validated the arguments.
+int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
+                  int wire_dtype, int variant, int grid_blocks, cudaStream_t stream, bool explicit_variant) {
+    Context &c = g_ctx;
+    if (nelem == 0) return AR_OK;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (dev != c.device) return AR_ERR_INVALID_ARG;
+
+    bool aligned = true;
+    bool alias = false;
+    for (int r = 0; r < c.R; ++r) aligned &= (reinterpret_cast<uintptr_t>(srcs[r]) % 16) == 0;
+    for (int d = 0; d < n_dsts; ++d) {
+        aligned &= (reinterpret_cast<uintptr_t>(dsts[d]) % 16) == 0;
+        for (int r = 0; r < c.R; ++r) alias |= (dsts[d] == srcs[r]);
+    }
+
+    const size_t esize = elem_bytes(dst_dtype);
+    if (variant == AR_VARIANT_AUTO) variant = c.forced_variant;
+    if (variant == AR_VARIANT_AUTO) {
+        const double bytes = static_cast<double>(c.R + n_dsts) * static_cast<double>(nelem) * esize;
+        variant = bytes < static_cast<double>(c.latency_max_bytes) ? AR_VARIANT_LATENCY : AR_VARIANT_BANDWIDTH;
+    }
+    if (!aligned && (variant == AR_VARIANT_LATENCY || variant == AR_VARIANT_BANDWIDTH)) {
+        if (explicit_variant) return AR_ERR_INVALID_ARG;
+        variant = AR_VARIANT_SCALAR;
+    }
+    if (c.fault_inject) return AR_ERR_CUDA;
+
+    ArParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r < c.R; ++r) p.src[r] = srcs[r];
+    for (int d = 0; d < n_dsts; ++d) p.dst[d] = dsts[d];
+    p.nelem = nelem;
+    p.R = c.R;
+    p.n_dsts = n_dsts;
+
+    // A destination that is also a source is written while it is being
+    // read, so those calls use coherent loads instead of the read-only path.
+    const int nc = alias ? 0 : 1;
+    const Kernels &k = kernels_for(dst_dtype, wire_dtype);
+    const size_t vec = 16 / esize;
+    const long long nvec = static_cast<long long>(nelem / vec);
+    const long long sms = c.sm_count;
+    KernelFn fn = nullptr;
+    int threads = 0, grid = 0;
+    switch (variant) {
+        case AR_VARIANT_LATENCY:
+            fn = k.latency[nc];
+            threads = kLatencyThreads;
+            grid = grid_cap((nvec + threads - 1) / threads, 0x7FFFFFFFll);
+            break;
+        case AR_VARIANT_BANDWIDTH: {
+            fn = k.bandwidth[nc];
+            threads = kBandwidthThreads;
+            const long long tile = static_cast<long long>(threads) * k.bandwidth_vecs_per_thread;
+            const int per_sm = c.bw_blocks_per_sm > 0 ? c.bw_blocks_per_sm : blocks_per_sm(fn, threads);
+            const long long cap = grid_blocks > 0 ? grid_blocks : sms * per_sm;
+            grid = grid_cap(grid_blocks > 0 ? cap : (nvec + tile - 1) / tile, cap);
+            break;
+        }
+        case AR_VARIANT_SCALAR: {
+            fn = k.scalar[nc];
+            threads = kScalarThreads;
+            const long long cap = grid_blocks > 0 ? grid_blocks : sms * blocks_per_sm(fn, threads);
+            grid = grid_cap(grid_blocks > 0 ? cap : (static_cast<long long>(nelem) + threads - 1) / threads, cap);
+            break;
+        }
+        case AR_VARIANT_NAIVE: {
+            fn = k.naive;
+            threads = kScalarThreads;
+            const long long cap = grid_blocks > 0 ? grid_blocks : sms * 16;
+            grid = grid_cap(grid_blocks > 0 ? cap : (static_cast<long long>(nelem) + threads - 1) / threads, cap);
+            break;
+        }
+        default: return AR_ERR_INVALID_ARG;
+    }
+
+    fn<<<grid, threads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    c.last_variant = variant;
+    return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ar_status_string(int status) {
+    switch (status) {
+        case AR_OK: return "ok";
+        case AR_ERR_INVALID_ARG: return "invalid argument";
+        case AR_ERR_UNSUPPORTED: return "unsupported dtype or device";
+        case AR_ERR_TOO_LARGE: return "nelem exceeds max_elems";
+        case AR_ERR_NOT_INITIALIZED: return "ar_init has not succeeded";
+        case AR_ERR_OVERLAP: return "a destination partly overlaps another buffer";
+        case AR_ERR_CUDA: return "CUDA call failed";
+        default: return "unknown status";
+    }
+}
+
+int ar_check_args(int R, const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, size_t max_elems,
+                  int dst_dtype, int wire_dtype) {
+    if (R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    if (n_dsts < 1 || n_dsts > AR_MAX_DSTS) return AR_ERR_INVALID_ARG;
+    if (!srcs || !dsts) return AR_ERR_INVALID_ARG;
+    const size_t esize = elem_bytes(dst_dtype);
+    if (!esize || !elem_bytes(wire_dtype)) return AR_ERR_UNSUPPORTED;
+    if (nelem > max_elems) return AR_ERR_TOO_LARGE;
+    if (nelem == 0) return AR_OK;
+    for (int r = 0; r < R; ++r) {
+        if (!srcs[r]) return AR_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(srcs[r]) % esize) return AR_ERR_INVALID_ARG;
+    }
+    for (int d = 0; d < n_dsts; ++d) {
+        if (!dsts[d]) return AR_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(dsts[d]) % esize) return AR_ERR_INVALID_ARG;
+    }
+    if (nelem > SIZE_MAX / esize) return AR_ERR_TOO_LARGE;
+    const size_t bytes = nelem * esize;
+    for (int d = 0; d < n_dsts; ++d) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dsts[d]);
+        if (a > UINTPTR_MAX - bytes) return AR_ERR_INVALID_ARG;
+        for (int r = 0; r < R; ++r) {
+            const uintptr_t b = reinterpret_cast<uintptr_t>(srcs[r]);
+            if (a != b && ranges_overlap(a, b, bytes)) return AR_ERR_OVERLAP;
+        }
+        for (int e = 0; e < d; ++e) {
+            if (ranges_overlap(a, reinterpret_cast<uintptr_t>(dsts[e]), bytes)) return AR_ERR_OVERLAP;
+        }
+    }
+    return AR_OK;
+}
+
+int ar_init(int R, size_t max_elems) {
+    if (R < 1 || R > AR_MAX_RANKS || max_elems < 1) return AR_ERR_INVALID_ARG;
+    if (max_elems > SIZE_MAX / 4) return AR_ERR_INVALID_ARG;
+    const int variant = parse_variant(getenv("AR_VARIANT"));
+    if (variant < 0) return AR_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_ctx = Context{};
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return AR_ERR_CUDA;
+    // The library carries sm_103a code only: make sure this device runs it.
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernels_for(AR_F32, AR_F32).latency[1])) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_UNSUPPORTED;
+    }
+    Context c;
+    c.R = R;
+    c.max_elems = max_elems;
+    c.device = dev;
+    c.sm_count = sms;
+    c.forced_variant = variant;
+    if (const char *s = getenv("AR_LATENCY_MAX_BYTES")) {
+        char *end = nullptr;
+        const long long v = strtoll(s, &end, 10);
+        if (end == s || v < 0) return AR_ERR_INVALID_ARG;
+        c.latency_max_bytes = v;
+    }
+    c.ready = true;
+    g_ctx = c;
+    if (const char *s = getenv("AR_LOG"); s && !strcmp(s, "1")) {
+        fprintf(stderr, "[ar] init: R=%d max_elems=%zu device=%d SMs=%d latency_max_bytes=%lld variant=%s\n", R,
+                max_elems, dev, sms, static_cast<long long>(c.latency_max_bytes), variant_name(variant));
+    }
+    return AR_OK;
+}
+
+void ar_free(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_ctx = Context{};
+}
+
+int ar_reduce_variant(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
+                      int wire_dtype, int variant, int grid_blocks, cudaStream_t stream) {
+    if (variant < AR_VARIANT_AUTO || variant > AR_VARIANT_SCALAR || grid_blocks < 0) return AR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    const int st = ar_check_args(g_ctx.R, srcs, dsts, n_dsts, nelem, g_ctx.max_elems, dst_dtype, wire_dtype);
+    if (st != AR_OK) return st;
+    return launch_locked(srcs, dsts, n_dsts, nelem, dst_dtype, wire_dtype, variant, grid_blocks, stream,
+                         variant != AR_VARIANT_AUTO);
+}
+
+int ar_reduce(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype, int wire_dtype,
+              cudaStream_t stream) {
+    return ar_reduce_variant(srcs, dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, stream);
+}
+
+int ar_query(int key, int64_t *value) {
+    if (!value) return AR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    const Context &c = g_ctx;
+    switch (key) {
+        case AR_Q_RANKS: *value = c.R; break;
+        case AR_Q_MAX_ELEMS: *value = static_cast<int64_t>(c.max_elems); break;
+        case AR_Q_DEVICE: *value = c.device; break;
+        case AR_Q_SM_COUNT: *value = c.sm_count; break;
+        case AR_Q_LATENCY_MAX_BYTES: *value = c.latency_max_bytes; break;
+        case AR_Q_FORCED_VARIANT: *value = c.forced_variant; break;
+        case AR_Q_LAST_VARIANT: *value = c.last_variant; break;
+        case AR_Q_FAULT_INJECT: *value = c.fault_inject; break;
+        case AR_Q_BW_BLOCKS_PER_SM: *value = c.bw_blocks_per_sm; break;
+        default: return AR_ERR_INVALID_ARG;
+    }
+    return AR_OK;
+}
+
+int ar_set_option(int key, int64_t value) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    Context &c = g_ctx;
+    switch (key) {
+        case AR_Q_LATENCY_MAX_BYTES:
+            if (value < 0) return AR_ERR_INVALID_ARG;
+            c.latency_max_bytes = value;
+            break;
+        case AR_Q_FORCED_VARIANT:
+            if (value < AR_VARIANT_AUTO || value > AR_VARIANT_SCALAR) return AR_ERR_INVALID_ARG;
+            c.forced_variant = static_cast<int>(value);
+            break;
+        case AR_Q_FAULT_INJECT: c.fault_inject = value ? 1 : 0; break;
+        case AR_Q_BW_BLOCKS_PER_SM:
+            if (value < 0 || value > 64) return AR_ERR_INVALID_ARG;
+            c.bw_blocks_per_sm = static_cast<int>(value);
+            break;
+        default: return AR_ERR_INVALID_ARG;
+    }
+    return AR_OK;
+}
+
+int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem, int dst_dtype,
+                   int wire_dtype, void *const *d_srcs, void *const *d_dsts, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    const Context &c = g_ctx;
+    if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
+    const void *srcs_c[AR_MAX_RANKS];
+    if (!d_srcs || c.R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < c.R; ++r) srcs_c[r] = d_srcs[r];
+    const int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+    if (st != AR_OK) return st;
+    if (nelem == 0) return AR_OK;
+    for (int r = 0; r < c.R; ++r)
+        if (!h_srcs[r]) return AR_ERR_INVALID_ARG;
+    for (int d = 0; d < n_dsts; ++d)
+        if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
+    if (c.fault_inject) return AR_ERR_CUDA;
+    const size_t bytes = nelem * elem_bytes(dst_dtype);
+    for (int r = 0; r < c.R; ++r)
+        if (cudaMemcpyAsync(d_srcs[r], h_srcs[r], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return AR_ERR_CUDA;
+    const int lst = launch_locked(srcs_c, d_dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, stream,
+                                  false);
+    if (lst != AR_OK) return lst;
+    for (int d = 0; d < n_dsts; ++d)
+        if (cudaMemcpyAsync(h_dsts[d], d_dsts[d], bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return AR_ERR_CUDA;
+    return AR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element
+by element, bit for bit (any NaN matches any NaN).
+
+Sizes are small enough for the oracle to finish in seconds yet span many
+16-byte vectors, several CTA tiles and a ragged tail."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_partial_sum_gb300 as tps
+from tensor_partial_sum_gb300 import workloads as W
+from tests.gpu_util import Ctx, check_guards, run, to_device, to_host
+from tests.libcasts import assert_same, lib_round
+from tests.test_oracle_fold import edgy_f32
+
+pytestmark = pytest.mark.gpu
+
+TYPES = ["f32", "f16", "bf16"]
+PAIRS = list(itertools.product(TYPES, TYPES))
+VARIANTS = ["auto", "latency", "bandwidth", "scalar", "naive"]
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_partial_sum_gb300 import build
+    build.build()
+    c = Ctx()
+    yield c
+    tps.ar_free()
+
+
+def srcs_for(seed, R, n, dst):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [lib_round(dst, edgy_f32(rng, n)) for _ in range(R)]
+
+
+def expect(srcs, dst, wire):
+    return oracle.reduce(srcs, 1, dst, wire)[0]
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8, 16])
+def test_all_pairs_all_variants(ctx, dst, wire, R):
+    n = 70001  # 17500 f32 vectors or 8750 16-bit vectors, plus a 1-element tail
+    srcs = srcs_for(R * 31 + len(dst), R, n, dst)
+    exp = expect(srcs, dst, wire)
+    n_dsts = R % 4 + 1
+    for v in VARIANTS:
+        outs, backs = run(ctx, srcs, n_dsts, dst, wire, variant=v, pad=256)
+        for d, o in enumerate(outs):
+            assert_same(o, exp, dst, f"{dst}/{wire} R={R} variant={v} dst={d}")
+        check_guards(backs)
+
+
+SIZES = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 33, 127, 128, 129, 255, 257, 1023, 1025,
+         4095, 4096, 4097, 4099, 256 * 4 * 4 - 1, 256 * 4 * 4 + 3, 1_000_003]
+
+
+@pytest.mark.parametrize("dst,wire", [("f32", "bf16"), ("bf16", "bf16"), ("f16", "f32")])
+@pytest.mark.parametrize("n", SIZES)
+def test_sizes_and_tails(ctx, dst, wire, n):
+    srcs = srcs_for(n, 4, n, dst)
+    exp = expect(srcs, dst, wire)
+    for v in VARIANTS:
+        outs, backs = run(ctx, srcs, 2, dst, wire, variant=v, pad=64)
+        for o in outs:
+            assert_same(o, exp, dst, f"n={n} variant={v}")
+        check_guards(backs)
+
+
+@pytest.mark.parametrize("variant", ["bandwidth", "scalar", "naive"])
+@pytest.mark.parametrize("grid", [1, 2, 3, 7, 152, 1000])
+def test_grid_size_does_not_change_bits(ctx, variant, grid):
+    n = 300_007
+    srcs = srcs_for(grid, 3, n, "f32")
+    exp = expect(srcs, "f32", "f16")
+    outs, _ = run(ctx, srcs, 1, "f32", "f16", variant=variant, grid=grid)
+    assert_same(outs[0], exp, "f32", f"{variant} grid={grid}")
+
+
+@pytest.mark.parametrize("dst", TYPES)
+def test_unaligned_pointers(ctx, dst):
+    """Buffers one element off 16-byte alignment take the element-wise path
+    and give the same bits; a forced vector variant is refused."""
+    n = 10_001
+    srcs = srcs_for(5, 3, n, dst)
+    exp = expect(srcs, dst, "bf16")
+    outs, backs = run(ctx, srcs, 2, dst, "bf16", src_offsets=[1, 0, 3], dst_offsets=[0, 1], pad=64)
+    for o in outs:
+        assert_same(o, exp, dst, "unaligned")
+    check_guards(backs)
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS["scalar"]
+    with pytest.raises(tps.ARError) as e:
+        run(ctx, srcs, 1, dst, "bf16", variant="bandwidth", src_offsets=[1, 0, 0])
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("k", [0, 2])
+def test_in_place(ctx, variant, k):
+    """A destination may be one of the sources (the pages reduce in place)."""
+    n = 50_003
+    srcs = srcs_for(7 + k, 3, n, "f32")
+    exp = expect(srcs, "f32", "bf16")
+    outs, _ = run(ctx, srcs, 2, "f32", "bf16", variant=variant, in_place=k)
+    for o in outs:
+        assert_same(o, exp, "f32", f"in place into source {k}")
+
+
+def test_auto_dispatch_by_size(ctx):
+    ctx.ensure(4, 1 << 22)
+    limit = tps.ar_query("latency_max_bytes")
+    small = max(1, limit // (8 * 4) - 64)
+    big = limit // (8 * 4) + 64
+    for n, want in ((small, "latency"), (big, "bandwidth")):
+        srcs = srcs_for(n, 4, n, "f32")
+        outs, _ = run(ctx, srcs, 4, "f32", "f16")
+        assert tps.ar_query("last_variant") == tps.ar.VARIANTS[want]
+        assert_same(outs[0], expect(srcs, "f32", "f16"), "f32", f"auto n={n}")
+
+
+def test_threshold_option_moves_dispatch(ctx):
+    ctx.ensure(2, 1 << 20)
+    old = tps.ar_query("latency_max_bytes")
+    try:
+        tps.ar_set_option("latency_max_bytes", 0)
+        srcs = srcs_for(1, 2, 1000, "f32")
+        run(ctx, srcs, 1, "f32", "bf16")
+        assert tps.ar_query("last_variant") == tps.ar.VARIANTS["bandwidth"]
+        tps.ar_set_option("latency_max_bytes", 1 << 40)
+        run(ctx, srcs, 1, "f32", "bf16")
+        assert tps.ar_query("last_variant") == tps.ar.VARIANTS["latency"]
+    finally:
+        tps.ar_set_option("latency_max_bytes", old)
+
+
+def test_zero_elements_is_a_no_op(ctx):
+    ctx.ensure(2, 1 << 16)
+    d = torch.full((8,), 3.0, device="cuda")
+    tps.ar_reduce([d, d], [d], nelem=0, dst_dtype="f32", wire_dtype="bf16")
+    torch.cuda.synchronize()
+    assert (d == 3.0).all()
+
+
+def test_errors_write_nothing(ctx):
+    ctx.ensure(2, 1000)
+    a = torch.randn(1000, device="cuda")
+    b = torch.randn(1000, device="cuda")
+    out = torch.full((1000,), 7.0, device="cuda")
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce([a, b], [out], nelem=1001, dst_dtype="f32")
+    assert e.value.status == 3
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce([a, b], [a[10:]], nelem=990, dst_dtype="f32")
+    assert e.value.status == 5
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce([a], [out], dst_dtype="f32")  # one source short of R=2
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()
+
+
+def test_fault_injection_returns_status_and_writes_nothing(ctx):
+    ctx.ensure(2, 1 << 16)
+    a = torch.randn(4096, device="cuda")
+    out = torch.full((4096,), 7.0, device="cuda")
+    tps.ar_set_option("fault_inject", 1)
+    try:
+        with pytest.raises(tps.ARError) as e:
+            tps.ar_reduce([a, a], [out], dst_dtype="f32")
+        assert e.value.status == 6
+    finally:
+        tps.ar_set_option("fault_inject", 0)
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()
+    tps.ar_reduce([a, a], [out], dst_dtype="f32")  # and the context still works
+    torch.cuda.synchronize()
+    assert torch.equal(out, (a.to(torch.bfloat16).float() * 2))
+
+
+def test_cuda_graph_capture_and_replay(ctx):
+    ctx.ensure(4, 1 << 16)
+    n = 4099
+    srcs = srcs_for(11, 4, n, "f32")
+    exp = expect(srcs, "f32", "f16")
+    src_t = [to_device(s, "f32") for s in srcs]
+    outs = [torch.zeros(n, device="cuda") for _ in range(4)]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        tps.ar_reduce(src_t, outs, dst_dtype="f32", wire_dtype="f16", stream=s)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for o in outs:
+        assert_same(to_host(o, "f32"), exp, "f32", "graph replay")
+    # replay again on new inputs written into the same buffers
+    srcs2 = srcs_for(12, 4, n, "f32")
+    for t, a in zip(src_t, srcs2):
+        t.copy_(to_device(a, "f32"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same(to_host(outs[3], "f32"), expect(srcs2, "f32", "f16"), "f32", "second replay")
+
+
+def test_host_entry_point(ctx):
+    """ar_reduce_host: pinned host partials in, host results out."""
+    w = W.WORKLOADS["tp_small"]
+    srcs = W.generate(w)
+    ctx.ensure(w.R, w.nelem)
+    exp = expect(srcs, w.dst, w.wire)
+    h_srcs = [torch.from_numpy(s).pin_memory() for s in srcs]
+    h_dsts = [torch.empty(w.nelem, dtype=torch.float32).pin_memory() for _ in range(w.n_dsts)]
+    d_srcs = [torch.empty(w.nelem, device="cuda") for _ in range(w.R)]
+    d_dsts = [torch.empty(w.nelem, device="cuda") for _ in range(w.n_dsts)]
+    tps.ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, dst_dtype="f32", wire_dtype=w.wire)
+    torch.cuda.synchronize()
+    for h in h_dsts:
+        assert_same(h.numpy(), exp, "f32", "host entry")
