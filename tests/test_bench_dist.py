@@ -1,0 +1,73 @@
+"""The benchmark's multi-rank plumbing on CPU with gloo, world size 2:
+barrier, max over ranks and the whole-job aggregate; and the reference arm
+under two ranks (rank 0 alone measures and prints)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    bench.dist_init(world, "gloo")
+    assert bench.dist_env() == (rank, rank, world)
+    bench.barrier()
+    # rank 1 is slower: the job time is the max over ranks
+    mx = bench.max_over_ranks(1.0 + rank)
+    gbs = bench.aggregate_gbs(1_000_000_000, 10, world, mx)
+    q.put((rank, mx, gbs))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_aggregate_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, mx, gbs in got:
+        assert mx == 2.0
+        assert gbs == pytest.approx(2 * 1e9 * 10 / 2.0 / 1e9)
+
+
+def test_single_rank_helpers_are_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.aggregate_gbs(2_000_000_000, 1, 1, 1.0) == 2.0
+
+
+def test_reference_arm_two_ranks_prints_once():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3", "--ref-seconds", "1",
+           "--workload", "tp_small"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["unit"] == "GB/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0

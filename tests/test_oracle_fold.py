@@ -45,7 +45,8 @@ def edgy_f32(rng, n):
     x = np.where(kind == 2, tiny, x)
     x = np.where(kind == 3, sub32, x)
     x = np.where(kind == 4, pick, x)
-    x = np.where(kind == 5, x * 1e4, x)
+    with np.errstate(over="ignore"):
+        x = np.where(kind == 5, x * np.float32(1e4), x)
     return x.astype(np.float32)
 
 
