@@ -34,7 +34,9 @@ METRIC = "effective HBM GB/s (% of roofline) prefill-size; µs/call decode-size"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ar_vec_kernel_prefill_traffic.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", f) for f in ("ar_kernels.cuh", "ar.cu")]
+KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", f)
+                  for f in ("ar_kernels.cuh", "ar_dispatch.h", "ar.cu", "ar_kernels_f32.cu", "ar_kernels_f16.cu",
+                            "ar_kernels_bf16.cu")]
 
 
 # ---- distributed plumbing (also exercised by the CPU tests with gloo) -------
@@ -237,6 +239,8 @@ def run_ours(args):
         sets.append((s, d))
     stream = torch.cuda.Stream(dev)
     tps.ar_init(w.R, w.nelem)
+    if args.bw_blocks_per_sm:
+        tps.ar_set_option("bw_blocks_per_sm", args.bw_blocks_per_sm)
 
     def step(i):
         s, d = sets[i % nsets]
@@ -468,6 +472,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=60.0)
     p.add_argument("--no-decode", dest="decode", action="store_false")
+    p.add_argument("--bw-blocks-per-sm", type=int, default=0,
+                   help="0: bandwidth grid covers the tensor; n: persistent grid of n CTAs per SM")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

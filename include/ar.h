@@ -85,8 +85,9 @@ typedef enum {
 typedef enum {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_NAIVE = 1,     /* one element per thread, grid-stride: a cross-check */
-    AR_VARIANT_LATENCY = 2,   /* one 16-byte vector per thread, one small launch */
-    AR_VARIANT_BANDWIDTH = 3, /* persistent grid, several vectors per thread */
+    AR_VARIANT_LATENCY = 2,   /* one 16-byte vector per thread, 128-thread CTAs */
+    AR_VARIANT_BANDWIDTH = 3, /* one 32-byte (f32) or 16-byte vector per thread, 256-thread
+                                 CTAs; all loads of two or four ranks issued together */
     AR_VARIANT_SCALAR = 4     /* element-wise path used for unaligned pointers */
 } ar_variant;
 
@@ -140,6 +141,8 @@ int ar_check_args(int R, const void *const *srcs, void *const *dsts, int n_dsts,
  *   variant     an ar_variant; AUTO behaves exactly like ar_reduce.
  *   grid_blocks CTAs to launch for BANDWIDTH/NAIVE/SCALAR (0 = the library's
  *               choice); ignored by LATENCY, whose grid covers the tensor.
+ *               A BANDWIDTH grid smaller than the tensor needs is persistent:
+ *               its CTAs sweep the tensors together in rounds.
  * The result bits do not depend on either argument.  A vector variant asked
  * for with unaligned pointers returns AR_ERR_INVALID_ARG.
  */
@@ -158,7 +161,8 @@ typedef enum {
     AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only) */
     AR_Q_FAULT_INJECT = 7,      /* nonzero: the next launches fail with AR_ERR_CUDA
                                    before anything is enqueued (host-side test hook) */
-    AR_Q_BW_BLOCKS_PER_SM = 8   /* resident CTAs per SM of the BANDWIDTH grid (0 = occupancy) */
+    AR_Q_BW_BLOCKS_PER_SM = 8   /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
+                                   persistent grid of n CTAs per SM (capped by occupancy) */
 } ar_key;
 
 /* Read one context value into *value.  AR_ERR_NOT_INITIALIZED before init. */

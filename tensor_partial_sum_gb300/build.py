@@ -17,13 +17,12 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libtps_ar.so")
-SOURCES = [os.path.join(CSRC, "ar.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "ar_kernels.cuh"), os.path.join(INCLUDE, "ar.h")]
+SOURCES = [os.path.join(CSRC, f) for f in ("ar.cu", "ar_kernels_f32.cu", "ar_kernels_f16.cu", "ar_kernels_bf16.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ar_kernels.cuh", "ar_dispatch.h")] + [os.path.join(INCLUDE, "ar.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-         "-I" + INCLUDE, "-I" + CSRC]
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
 
 def stale() -> bool:
@@ -34,19 +33,25 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit in parallel, then link the shared
+    library (written under a temporary name and renamed into place)."""
     if not force and not stale():
         return LIB
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=HERE)
-    os.close(fd)
-    cmd = [NVCC, *ARCH, *FLAGS, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    try:
-        subprocess.run(cmd, check=True)
+    with tempfile.TemporaryDirectory(dir=HERE, prefix="_build_") as tmpdir:
+        objs, procs = [], []
+        for src in SOURCES:
+            obj = os.path.join(tmpdir, os.path.basename(src) + ".o")
+            cmd = [NVCC, *ARCH, *FLAGS, "-c", "-o", obj, src]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            procs.append(subprocess.Popen(cmd))
+            objs.append(obj)
+        codes = [p.wait() for p in procs]
+        if any(codes):
+            raise RuntimeError(f"nvcc failed ({codes})")
+        tmp = os.path.join(tmpdir, "libtps_ar.so")
+        subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], check=True)
         os.replace(tmp, LIB)
-    finally:
-        if os.path.exists(tmp):
-            os.unlink(tmp)
     return LIB
 
 

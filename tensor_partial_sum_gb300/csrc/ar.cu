@@ -17,7 +17,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "ar_kernels.cuh"
+#include "ar_dispatch.h"
 
 using tps::ArParams;
 
@@ -55,49 +55,13 @@ size_t elem_bytes(int dtype) {
 
 bool ranges_overlap(uintptr_t a, uintptr_t b, size_t bytes) { return a < b + bytes && b < a + bytes; }
 
-// ---- kernel tables, indexed [dst dtype][wire dtype] ------------------------
-using KernelFn = void (*)(ArParams);
-
-template <int Td, int Tw>
-struct KernelSet {
-    static constexpr int kU = (Td == tps::kF32) ? 4 : 2;  // 64 or 32 bytes per thread per rank
-    static constexpr KernelFn latency[2] = {tps::ar_vec_kernel<Td, Tw, 1, false>,
-                                            tps::ar_vec_kernel<Td, Tw, 1, true>};
-    static constexpr KernelFn bandwidth[2] = {tps::ar_vec_kernel<Td, Tw, kU, false>,
-                                              tps::ar_vec_kernel<Td, Tw, kU, true>};
-    static constexpr KernelFn scalar[2] = {tps::ar_scalar_kernel<Td, Tw, false>,
-                                           tps::ar_scalar_kernel<Td, Tw, true>};
-    static constexpr KernelFn naive = tps::ar_naive_kernel<Td, Tw>;
-};
-
-struct Kernels {
-    KernelFn latency[2];
-    KernelFn bandwidth[2];
-    KernelFn scalar[2];
-    KernelFn naive;
-    int bandwidth_vecs_per_thread;
-};
-
-template <int Td, int Tw>
-Kernels make_kernels() {
-    using S = KernelSet<Td, Tw>;
-    return Kernels{{S::latency[0], S::latency[1]},
-                   {S::bandwidth[0], S::bandwidth[1]},
-                   {S::scalar[0], S::scalar[1]},
-                   S::naive,
-                   S::kU};
-}
+using tps::KernelFn;
+using tps::Kernels;
 
 const Kernels &kernels_for(int dst, int wire) {
-    static const Kernels table[3][3] = {
-        {make_kernels<tps::kF32, tps::kF32>(), make_kernels<tps::kF32, tps::kF16>(),
-         make_kernels<tps::kF32, tps::kBF16>()},
-        {make_kernels<tps::kF16, tps::kF32>(), make_kernels<tps::kF16, tps::kF16>(),
-         make_kernels<tps::kF16, tps::kBF16>()},
-        {make_kernels<tps::kBF16, tps::kF32>(), make_kernels<tps::kBF16, tps::kF16>(),
-         make_kernels<tps::kBF16, tps::kBF16>()},
-    };
-    return table[dst][wire];
+    if (dst == AR_F32) return tps::kernels_f32(wire);
+    if (dst == AR_F16) return tps::kernels_f16(wire);
+    return tps::kernels_bf16(wire);
 }
 
 // Resident CTAs per SM of a kernel (queried once per kernel, then cached).
@@ -155,13 +119,15 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
     if (dev != c.device) return AR_ERR_INVALID_ARG;
 
-    bool aligned = true;
+    uintptr_t any_bits = 0;  // OR of all addresses: its low bits give the common alignment
     bool alias = false;
-    for (int r = 0; r < c.R; ++r) aligned &= (reinterpret_cast<uintptr_t>(srcs[r]) % 16) == 0;
+    for (int r = 0; r < c.R; ++r) any_bits |= reinterpret_cast<uintptr_t>(srcs[r]);
     for (int d = 0; d < n_dsts; ++d) {
-        aligned &= (reinterpret_cast<uintptr_t>(dsts[d]) % 16) == 0;
+        any_bits |= reinterpret_cast<uintptr_t>(dsts[d]);
         for (int r = 0; r < c.R; ++r) alias |= (dsts[d] == srcs[r]);
     }
+    const bool aligned = (any_bits % 16) == 0;
+    const bool aligned32 = (any_bits % 32) == 0;
 
     const size_t esize = elem_bytes(dst_dtype);
     if (variant == AR_VARIANT_AUTO) variant = c.forced_variant;
@@ -187,24 +153,37 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     // read, so those calls use coherent loads instead of the read-only path.
     const int nc = alias ? 0 : 1;
     const Kernels &k = kernels_for(dst_dtype, wire_dtype);
-    const size_t vec = 16 / esize;
-    const long long nvec = static_cast<long long>(nelem / vec);
     const long long sms = c.sm_count;
     KernelFn fn = nullptr;
     int threads = 0, grid = 0;
     switch (variant) {
-        case AR_VARIANT_LATENCY:
-            fn = k.latency[nc];
+        case AR_VARIANT_LATENCY: {
+            // 16-byte vectors, one per thread, a grid that covers the tensor
+            const tps::VecKernels &vk = k.v16;
+            fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kLatencyThreads;
-            grid = grid_cap((nvec + threads - 1) / threads, 0x7FFFFFFFll);
+            const long long nv = static_cast<long long>(nelem / (16 / esize));
+            grid = grid_cap((nv + threads - 1) / threads, 0x7FFFFFFFll);
             break;
+        }
         case AR_VARIANT_BANDWIDTH: {
-            fn = k.bandwidth[nc];
+            // the widest vectors every pointer is aligned for, one per thread;
+            // a grid that covers the tensor unless a persistent grid is asked for
+            const bool wide = k.wide_bytes == 32 && aligned32;
+            const tps::VecKernels &vk = wide ? k.wide : k.v16;
+            const int vec_bytes = wide ? k.wide_bytes : 16;
+            fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kBandwidthThreads;
-            const long long tile = static_cast<long long>(threads) * k.bandwidth_vecs_per_thread;
-            const int per_sm = c.bw_blocks_per_sm > 0 ? c.bw_blocks_per_sm : blocks_per_sm(fn, threads);
-            const long long cap = grid_blocks > 0 ? grid_blocks : sms * per_sm;
-            grid = grid_cap(grid_blocks > 0 ? cap : (nvec + tile - 1) / tile, cap);
+            const long long nv = static_cast<long long>(nelem / (vec_bytes / esize));
+            const long long full = (nv + threads - 1) / threads;
+            if (grid_blocks > 0) {
+                grid = grid_blocks;
+            } else if (c.bw_blocks_per_sm > 0) {
+                const int occ = blocks_per_sm(fn, threads);
+                grid = grid_cap(full, sms * (c.bw_blocks_per_sm < occ ? c.bw_blocks_per_sm : occ));
+            } else {
+                grid = grid_cap(full, 0x7FFFFFFFll);
+            }
             break;
         }
         case AR_VARIANT_SCALAR: {
@@ -293,7 +272,7 @@ int ar_init(int R, size_t max_elems) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return AR_ERR_CUDA;
     // The library carries sm_103a code only: make sure this device runs it.
     cudaFuncAttributes attr;
-    if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernels_for(AR_F32, AR_F32).latency[1])) !=
+    if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernels_for(AR_F32, AR_F32).v16.few[1])) !=
         cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_UNSUPPORTED;

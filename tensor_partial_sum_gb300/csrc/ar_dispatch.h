@@ -1,0 +1,56 @@
+// Host-side view of the kernel instantiations: one table per (dst, wire)
+// type pair, filled by the per-type translation units (ar_kernels_*.cu).
+#pragma once
+
+#include "ar_kernels.cuh"
+
+namespace tps {
+
+using KernelFn = void (*)(ArParams);
+
+// One vector width with its two rank-batch sizes, each as [NC] pair
+// (0 = coherent loads because a destination is also a source, 1 = read-only
+// loads).
+struct VecKernels {
+    KernelFn few[2];   // R <= 2: ranks loaded two at a time
+    KernelFn many[2];  // R >= 3: ranks loaded four at a time
+};
+
+struct Kernels {
+    VecKernels v16;    // 16-byte vectors
+    VecKernels wide;   // the bandwidth width: 32-byte vectors for f32, 16 for 16-bit types
+    int wide_bytes;    // 32 or 16
+    KernelFn scalar[2];  // [NC]
+    KernelFn naive;
+};
+
+// Defined in ar_kernels_f32.cu / ar_kernels_f16.cu / ar_kernels_bf16.cu.
+const Kernels &kernels_f32(int wire);
+const Kernels &kernels_f16(int wire);
+const Kernels &kernels_bf16(int wire);
+
+template <int Td, int Tw, int VB>
+VecKernels make_vec_kernels() {
+    return VecKernels{{ar_reduce_kernel<Td, Tw, VB, 1, 2, false>, ar_reduce_kernel<Td, Tw, VB, 1, 2, true>},
+                      {ar_reduce_kernel<Td, Tw, VB, 1, 4, false>, ar_reduce_kernel<Td, Tw, VB, 1, 4, true>}};
+}
+
+// Kernel set of one (dst, wire) pair.
+template <int Td, int Tw>
+Kernels make_kernels() {
+    Kernels k{};
+    k.v16 = make_vec_kernels<Td, Tw, 16>();
+    if constexpr (Td == kF32) {
+        k.wide = make_vec_kernels<Td, Tw, 32>();
+        k.wide_bytes = 32;
+    } else {
+        k.wide = k.v16;
+        k.wide_bytes = 16;
+    }
+    k.scalar[0] = ar_scalar_kernel<Td, Tw, false>;
+    k.scalar[1] = ar_scalar_kernel<Td, Tw, true>;
+    k.naive = ar_naive_kernel<Td, Tw>;
+    return k;
+}
+
+}  // namespace tps

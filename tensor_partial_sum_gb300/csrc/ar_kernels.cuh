@@ -34,6 +34,15 @@ struct ArParams {
     int n_dsts;
 };
 
+// Programmatic dependent launch: when a launch opts in, the next kernel on
+// the stream may start while this one runs; griddepcontrol.wait then holds
+// it until this grid has completed and its writes are visible, so results
+// never depend on the overlap.  Without the opt-in both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int T>
 struct Elem;
 template <>
@@ -114,51 +123,6 @@ __device__ __forceinline__ void wire2(float &a, float &b) {
     }
 }
 
-// ---- 16-byte vectors ----------------------------------------------------
-template <int Td>
-constexpr int kVec = 16 / Elem<Td>::bytes;
-
-template <bool NC>
-__device__ __forceinline__ uint4 load16(const uint4 *p) {
-    if constexpr (NC) {
-        uint4 v;
-        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-            : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-            : "l"(p));
-        return v;
-    } else {
-        return *p;
-    }
-}
-
-// The operands of one 16-byte source vector, rounded through the wire type.
-template <int Td, int Tw>
-__device__ __forceinline__ void operands(const uint4 &v, float (&x)[kVec<Td>]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if constexpr (Td == kF32) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(w[k]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) widen2<Td>(w[k], x[2 * k], x[2 * k + 1]);
-    }
-#pragma unroll
-    for (int k = 0; k < kVec<Td>; k += 2) wire2<Td, Tw>(x[k], x[k + 1]);
-}
-
-template <int Td>
-__device__ __forceinline__ uint4 pack_result(const float (&acc)[kVec<Td>]) {
-    uint32_t w[4];
-    if constexpr (Td == kF32) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[k] = __float_as_uint(acc[k]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[k] = narrow2<Td>(acc[2 * k], acc[2 * k + 1]);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // ---- one element at a time ----------------------------------------------
 template <int Td, bool NC>
 __device__ __forceinline__ float load_elem(const void *base, size_t i) {
@@ -200,57 +164,161 @@ __device__ __forceinline__ void reduce_elem(const ArParams &p, size_t i) {
 
 // ---- kernels ------------------------------------------------------------
 
-// Vector kernel: each thread owns U 16-byte vectors per tile (one per
-// blockDim.x stride, so every load instruction of a warp covers 512
-// contiguous bytes).  U = 1 with a grid covering the tensor is the latency
-// variant; larger U with a grid of a few CTAs per SM that strides over tiles
-// is the bandwidth variant.  The last CTA also does the tail of fewer than
-// one vector's worth of elements, element by element.
-template <int Td, int Tw, int U, bool NC>
-__global__ void __launch_bounds__(256) ar_vec_kernel(const __grid_constant__ ArParams p) {
-    constexpr int V = kVec<Td>;
-    const size_t nvec = p.nelem / V;
-    const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x * U;
-    for (size_t base = static_cast<size_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; base < nvec;
-         base += step) {
+// ---- words of a wide vector ----------------------------------------------
+// A vector of VB bytes (16 or 32) held as VB/4 32-bit words.  32-byte
+// accesses (ld/st .v8.b32) need 32-byte-aligned addresses and halve the
+// number of memory instructions per byte.
+template <int VB, bool NC>
+__device__ __forceinline__ void load_words(const void *p, uint32_t (&w)[VB / 4]) {
+    static_assert(VB == 16 || VB == 32, "vector width");
+    if constexpr (VB == 16) {
+        if constexpr (NC) {
+            asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                : "l"(p));
+        } else {
+            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "l"(p)
+                         : "memory");
+        }
+    } else {
+        if constexpr (NC) {
+            asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                  "=r"(w[7])
+                : "l"(p));
+        } else {
+            asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                           "=r"(w[7])
+                         : "l"(p)
+                         : "memory");
+        }
+    }
+}
+
+template <int VB>
+__device__ __forceinline__ void store_words(void *p, const uint32_t (&w)[VB / 4]) {
+    if constexpr (VB == 16) {
+        asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                     "r"(w[3])
+                     : "memory");
+    } else {
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    }
+}
+
+// The operands held in NW words of T_dst, rounded through the wire type.
+template <int Td, int Tw, int NW>
+__device__ __forceinline__ void word_operands(const uint32_t (&w)[NW], float (&x)[NW * 4 / Elem<Td>::bytes]) {
+    if constexpr (Td == kF32) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) x[k] = __uint_as_float(w[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) widen2<Td>(w[k], x[2 * k], x[2 * k + 1]);
+    }
+#pragma unroll
+    for (int k = 0; k < NW * 4 / Elem<Td>::bytes; k += 2) wire2<Td, Tw>(x[k], x[k + 1]);
+}
+
+template <int Td, int NW>
+__device__ __forceinline__ void word_pack(const float (&acc)[NW * 4 / Elem<Td>::bytes], uint32_t (&w)[NW]) {
+    if constexpr (Td == kF32) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = __float_as_uint(acc[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = narrow2<Td>(acc[2 * k], acc[2 * k + 1]);
+    }
+}
+
+// The vectors [first, end) of one thread block, RB ranks per batch, U
+// vectors per thread per tile; see ar_bw_kernel.
+template <int Td, int Tw, int VB, int U, int RB, bool NC>
+__device__ __forceinline__ void reduce_span(const ArParams &p, size_t first, size_t end) {
+    constexpr int NW = VB / 4;
+    constexpr int V = VB / Elem<Td>::bytes;
+    const size_t tile = static_cast<size_t>(blockDim.x) * U;
+    for (size_t base = first + threadIdx.x; base < end; base += tile) {
         float acc[U][V];
-        {
-            const uint4 *s = static_cast<const uint4 *>(p.src[0]);
-            uint4 v[U];
+        for (int r0 = 0; r0 < p.R; r0 += RB) {
+            uint32_t w[RB][U][NW];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t idx = base + static_cast<size_t>(u) * blockDim.x;
-                v[u] = idx < nvec ? load16<NC>(s + idx) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < RB; ++j) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const size_t idx = base + static_cast<size_t>(u) * blockDim.x;
+                    if (r0 + j < p.R && idx < end) {
+                        load_words<VB, NC>(static_cast<const char *>(p.src[r0 + j]) + idx * VB, w[j][u]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < NW; ++k) w[j][u][k] = 0u;
+                    }
+                }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) operands<Td, Tw>(v[u], acc[u]);
+            for (int j = 0; j < RB; ++j) {
+                if (r0 + j < p.R) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        float x[V];
+                        word_operands<Td, Tw, NW>(w[j][u], x);
+                        if (r0 + j == 0) {
+#pragma unroll
+                            for (int k = 0; k < V; ++k) acc[u][k] = x[k];
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < V; ++k) acc[u][k] = __fadd_rn(acc[u][k], x[k]);
+                        }
+                    }
+                }
+            }
         }
-        for (int r = 1; r < p.R; ++r) {
-            const uint4 *s = static_cast<const uint4 *>(p.src[r]);
-            uint4 v[U];
+        uint32_t out[U][NW];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t idx = base + static_cast<size_t>(u) * blockDim.x;
-                v[u] = idx < nvec ? load16<NC>(s + idx) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float x[V];
-                operands<Td, Tw>(v[u], x);
-#pragma unroll
-                for (int k = 0; k < V; ++k) acc[u][k] = __fadd_rn(acc[u][k], x[k]);
-            }
-        }
-        uint4 out[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) out[u] = pack_result<Td>(acc[u]);
+        for (int u = 0; u < U; ++u) word_pack<Td, NW>(acc[u], out[u]);
         for (int d = 0; d < p.n_dsts; ++d) {
-            uint4 *o = static_cast<uint4 *>(p.dst[d]);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const size_t idx = base + static_cast<size_t>(u) * blockDim.x;
-                if (idx < nvec) __stcs(o + idx, out[u]);
+                if (idx < end) store_words<VB>(static_cast<char *>(p.dst[d]) + idx * VB, out[u]);
             }
+        }
+    }
+}
+
+// The reduction kernel.  G CTAs of T threads cover nvec vectors of VB bytes
+// in K = ceil(nvec / (G*T*U)) rounds: in round k, CTA b takes the c vectors
+// starting at (k*G + b)*c, with c = ceil(nvec / (K*G)) <= T*U.  Launched
+// with G = ceil(nvec / (T*U)) this is one round and one vector (U = 1) per
+// thread, and the hardware block scheduler balances the CTAs; launched with
+// a smaller, persistent grid the CTAs move through the tensors together in
+// one window and each CTA's total differs from the others' by at most one
+// chunk.  Ranks are loaded RB at a time: all RB*U loads of a batch are
+// issued before the first conversion (RB*U*VB bytes in flight per thread),
+// then the batch's operands are added in ascending rank order.  Each warp
+// access covers 32 adjacent vectors.  The last CTA also does the tail of
+// fewer than one vector's elements.
+template <int Td, int Tw, int VB, int U, int RB, bool NC>
+__global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ ArParams p) {
+    constexpr int V = VB / Elem<Td>::bytes;
+    const size_t nvec = p.nelem / V;
+    const size_t G = gridDim.x;
+    const size_t b = blockIdx.x;
+    const size_t tile = static_cast<size_t>(blockDim.x) * U;
+    pdl_launch_dependents();
+    pdl_wait();
+    if (nvec > 0) {
+        const size_t K = (nvec + G * tile - 1) / (G * tile);
+        const size_t c = (nvec + K * G - 1) / (K * G);
+        for (size_t k = 0; k < K; ++k) {
+            const size_t first = (k * G + b) * c;
+            if (first >= nvec) break;
+            reduce_span<Td, Tw, VB, U, RB, NC>(p, first, first + c < nvec ? first + c : nvec);
         }
     }
     if (blockIdx.x == gridDim.x - 1) {
@@ -260,7 +328,7 @@ __global__ void __launch_bounds__(256) ar_vec_kernel(const __grid_constant__ ArP
 }
 
 // Element-wise grid-stride kernel: the path for pointers that are not all
-// 16-byte aligned.  Same arithmetic as the vector kernel, one element per
+// 16-byte aligned.  Same arithmetic as ar_reduce_kernel, one element per
 // thread per iteration.
 template <int Td, int Tw, bool NC>
 __global__ void __launch_bounds__(256) ar_scalar_kernel(const __grid_constant__ ArParams p) {

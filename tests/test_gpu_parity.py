@@ -225,3 +225,37 @@ def test_host_entry_point(ctx):
     torch.cuda.synchronize()
     for h in h_dsts:
         assert_same(h.numpy(), exp, "f32", "host entry")
+
+
+@pytest.mark.parametrize("dst", TYPES)
+@pytest.mark.parametrize("R", [2, 5])
+def test_sixteen_but_not_32_byte_aligned(ctx, dst, R):
+    """Pointers 16-byte aligned but not 32-byte aligned take the 16-byte
+    vectors of the bandwidth variant; same bits."""
+    n = 100_003
+    shift = 16 // (4 if dst == "f32" else 2)  # one 16-byte step, in elements
+    srcs = srcs_for(R + 40, R, n, dst)
+    exp = expect(srcs, dst, "f16")
+    outs, backs = run(ctx, srcs, 2, dst, "f16", variant="bandwidth", src_offsets=[shift] + [0] * (R - 1),
+                      dst_offsets=[0, shift], pad=64)
+    for o in outs:
+        assert_same(o, exp, dst, "16-byte aligned")
+    check_guards(backs)
+
+
+@pytest.mark.parametrize("per_sm", [1, 2, 3])
+@pytest.mark.parametrize("dst,R", [("f32", 2), ("f32", 8), ("bf16", 4)])
+def test_persistent_grid_option(ctx, per_sm, dst, R):
+    """A persistent bandwidth grid (CTAs sweep the tensors in rounds) gives
+    the same bits as the covering grid."""
+    n = 1_000_003
+    srcs = srcs_for(per_sm * 7 + R, R, n, dst)
+    exp = expect(srcs, dst, "bf16")
+    ctx.ensure(R, n)
+    tps.ar_set_option("bw_blocks_per_sm", per_sm)
+    try:
+        outs, _ = run(ctx, srcs, 2, dst, "bf16", variant="bandwidth")
+    finally:
+        tps.ar_set_option("bw_blocks_per_sm", 0)
+    for o in outs:
+        assert_same(o, exp, dst, f"persistent per_sm={per_sm}")
