@@ -321,31 +321,40 @@ def run_ours(args):
         "clocks": clocks,
     }
 
-    # end to end through the host entry point: pinned host partials in, results out
+    # end to end through the host entry point: pinned host partials in,
+    # pinned host results out, every step inside the timed region
     if args.e2e_steps > 0:
         h_srcs = [torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory() for a in srcs_np]
         h_dsts = [torch.empty(w.nelem, dtype=h_srcs[0].dtype).pin_memory() for _ in range(w.n_dsts)]
         d_srcs, d_dsts = sets[0]
 
-        def e2e_step():
-            tps.ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, nelem=w.nelem, dst_dtype=w.dst,
-                               wire_dtype=w.wire, stream=stream)
+        def e2e_time(staged: bool) -> float:
+            def one():
+                tps.ar_reduce_host(h_srcs, h_dsts, d_srcs if staged else None, d_dsts if staged else None,
+                                   nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire, stream=stream)
+            for _ in range(3):
+                one()
+            torch.cuda.synchronize(dev)
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.e2e_steps):
+                one()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return max_over_ranks(a.elapsed_time(b) / 1e3, dev)
 
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        e_el = max_over_ranks(a.elapsed_time(b) / 1e3, dev)
-        result["e2e"] = {"value": round(aggregate_gbs(w.bytes_per_call, args.e2e_steps, world, e_el), 2),
+        direct = e2e_time(staged=False)
+        staged = e2e_time(staged=True)
+        result["e2e"] = {"value": round(aggregate_gbs(w.bytes_per_call, args.e2e_steps, world, direct), 2),
                          "unit": UNIT, "h2d_bytes_per_step": w.R * w.nelem * w.elem_bytes,
                          "d2h_bytes_per_step": w.n_dsts * w.nelem * w.elem_bytes, "steps": args.e2e_steps,
-                         "call": "ar_reduce_host (pinned host buffers)"}
+                         "call": "ar_reduce_host without staging: the kernel loads the pinned host partials and "
+                                 "stores the pinned host results over NVLink-C2C",
+                         "staged_pipeline_value": round(aggregate_gbs(w.bytes_per_call, args.e2e_steps, world,
+                                                                      staged), 2),
+                         "staged_pipeline_call": "ar_reduce_host with device staging: chunked H2D copy, kernel, "
+                                                 "D2H copy on three streams"}
 
     del sets, base_src
     torch.cuda.empty_cache()

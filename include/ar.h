@@ -33,9 +33,10 @@
  *     pages are silent.
  *
  * Conventions for every call below:
- *   - Device pointers are plain CUDA device addresses on the device that was
- *     current at ar_init; host pointers are ordinary (ideally pinned) host
- *     memory.  The caller owns every buffer and the stream; the library
+ *   - Device pointers are CUDA addresses the device that was current at
+ *     ar_init can access: device memory, or pinned/managed host memory
+ *     (which the kernel then reads or writes over the CPU-GPU link); host
+ *     pointers are ordinary (ideally pinned) host memory.  The caller owns every buffer and the stream; the library
  *     keeps no pointer after a call returns and allocates nothing per call.
  *   - Calls that take a stream only enqueue work on it and return; results
  *     are ready when the stream reaches that point.  No call synchronizes,
@@ -161,8 +162,10 @@ typedef enum {
     AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only) */
     AR_Q_FAULT_INJECT = 7,      /* nonzero: the next launches fail with AR_ERR_CUDA
                                    before anything is enqueued (host-side test hook) */
-    AR_Q_BW_BLOCKS_PER_SM = 8   /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
+    AR_Q_BW_BLOCKS_PER_SM = 8,  /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
                                    persistent grid of n CTAs per SM (capped by occupancy) */
+    AR_Q_HOST_CHUNK_BYTES = 9   /* ar_reduce_host pipeline chunk, bytes per buffer (default 4 MiB;
+                                   at most 64 chunks per call) */
 } ar_key;
 
 /* Read one context value into *value.  AR_ERR_NOT_INITIALIZED before init. */
@@ -174,14 +177,27 @@ int ar_set_option(int key, int64_t value);
 
 /*
  * ar_reduce_host -- the same reduction for callers whose partials live in
- * host memory: copies each host source into the caller's device staging
- * buffer, reduces into the caller's device destination buffers, and copies
- * every destination back to its host buffer, all enqueued on `stream`.
- *   h_srcs, h_dsts  R and n_dsts host pointers (pinned memory makes the
- *                   copies asynchronous; pageable memory also works).
- *   d_srcs, d_dsts  R and n_dsts device buffers of nelem elements each.
- * Everything else as for ar_reduce.  The host results are valid once the
- * stream has reached the end of this call.
+ * host memory; the results are written back to host memory.
+ *   h_srcs, h_dsts  R and n_dsts host pointers, nelem elements each.
+ * Two ways to move the data, chosen by the staging arguments:
+ *   d_srcs, d_dsts  R and n_dsts device buffers of nelem elements: each host
+ *                   source is copied into its staging buffer, the reduction
+ *                   writes the staging destinations, and those are copied
+ *                   back to the host.  The work is cut into chunks (see
+ *                   AR_Q_HOST_CHUNK_BYTES) and pipelined over three streams
+ *                   the context owns, so copies in, kernels and copies out of
+ *                   different chunks overlap.  Pinned host memory makes the
+ *                   copies asynchronous; pageable memory also works.
+ *   both NULL       no staging: the kernel itself loads the host partials and
+ *                   stores the host results over the CPU-GPU link (NVLink-C2C
+ *                   on GB300), with no copies at all.  Every host buffer must
+ *                   be memory the GPU can reach (cudaHostAlloc /
+ *                   cudaHostRegister pinned memory, or managed memory);
+ *                   otherwise AR_ERR_INVALID_ARG.
+ * Everything else as for ar_reduce.  Either way the work starts after what
+ * is already enqueued on `stream`, and `stream` reaches the end of this
+ * call only when the host results are complete.  Results are identical to
+ * one ar_reduce over device copies of the same tensors.
  */
 int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem,
                    int dst_dtype, int wire_dtype, void *const *d_srcs, void *const *d_dsts,

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3:
                 4: "AR_ERR_NOT_INITIALIZED", 5: "AR_ERR_OVERLAP", 6: "AR_ERR_CUDA"}
 VARIANTS = {"auto": 0, "naive": 1, "latency": 2, "bandwidth": 3, "scalar": 4}
 KEYS = {"ranks": 0, "max_elems": 1, "device": 2, "sm_count": 3, "latency_max_bytes": 4,
-        "forced_variant": 5, "last_variant": 6, "fault_inject": 7, "bw_blocks_per_sm": 8}
+        "forced_variant": 5, "last_variant": 6, "fault_inject": 7, "bw_blocks_per_sm": 8,
+        "host_chunk_bytes": 9}
 
 _lib = None
 
@@ -176,10 +177,11 @@ def ar_set_option(key, value: int) -> None:
     _check(lib().ar_set_option(k, value), "ar_set_option")
 
 
-def ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, nelem=None, dst_dtype=None, wire_dtype="bf16",
+def ar_reduce_host(h_srcs, h_dsts, d_srcs=None, d_dsts=None, nelem=None, dst_dtype=None, wire_dtype="bf16",
                    stream=None) -> None:
-    """Host partials in, host results out, through the caller's device
-    staging buffers; everything is enqueued on ``stream``."""
-    nelem, dcode = _infer(d_srcs, nelem, dst_dtype)
+    """Host partials in, host results out: through the caller's device
+    staging buffers, or (``d_srcs``/``d_dsts`` None) with the kernel reading
+    and writing the pinned host buffers directly; ordered on ``stream``."""
+    nelem, dcode = _infer(d_srcs if d_srcs is not None else h_srcs, nelem, dst_dtype)
     _check(lib().ar_reduce_host(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode, _dtype_code(wire_dtype),
                                 _ptrs(d_srcs), _ptrs(d_dsts), _stream(stream)), "ar_reduce_host")

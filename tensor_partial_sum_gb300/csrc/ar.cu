@@ -27,6 +27,19 @@ constexpr int kLatencyThreads = 128;
 constexpr int kBandwidthThreads = 256;
 constexpr int kScalarThreads = 256;
 constexpr int64_t kDefaultLatencyMaxBytes = 4ll << 20;
+// ar_reduce_host cuts a call into chunks of this many bytes per buffer (at
+// most kMaxHostChunks chunks) so that host->device copies, kernels and
+// device->host copies of different chunks overlap.
+constexpr int64_t kDefaultHostChunkBytes = 4ll << 20;
+constexpr int kMaxHostChunks = 64;
+
+// Streams and events of the ar_reduce_host pipeline, made once at ar_init.
+struct HostPipe {
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t copied[kMaxHostChunks] = {};
+    cudaEvent_t reduced[kMaxHostChunks] = {};
+};
 
 struct Context {
     bool ready = false;
@@ -39,7 +52,34 @@ struct Context {
     int last_variant = AR_VARIANT_AUTO;
     int fault_inject = 0;
     int bw_blocks_per_sm = 0;
+    int64_t host_chunk_bytes = kDefaultHostChunkBytes;
+    HostPipe pipe;
 };
+
+void destroy_pipe(HostPipe &p) {
+    for (cudaStream_t *s : {&p.h2d, &p.comp, &p.d2h})
+        if (*s) cudaStreamDestroy(*s), *s = nullptr;
+    for (cudaEvent_t *e : {&p.start, &p.done})
+        if (*e) cudaEventDestroy(*e), *e = nullptr;
+    for (int k = 0; k < kMaxHostChunks; ++k) {
+        if (p.copied[k]) cudaEventDestroy(p.copied[k]), p.copied[k] = nullptr;
+        if (p.reduced[k]) cudaEventDestroy(p.reduced[k]), p.reduced[k] = nullptr;
+    }
+}
+
+bool create_pipe(HostPipe &p) {
+    const unsigned ev = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.start, ev) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.done, ev) == cudaSuccess;
+    for (int k = 0; ok && k < kMaxHostChunks; ++k)
+        ok = cudaEventCreateWithFlags(&p.copied[k], ev) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p.reduced[k], ev) == cudaSuccess;
+    if (!ok) destroy_pipe(p);
+    return ok;
+}
 
 std::mutex g_mu;
 Context g_ctx;
@@ -209,6 +249,51 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     return AR_OK;
 }
 
+// Device address of host memory the GPU can reach (pinned or managed), or
+// nullptr for memory it cannot (pageable, or unknown to CUDA).
+void *device_view(const void *host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeManaged) return const_cast<void *>(host);
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
+// ar_reduce_host without staging buffers: the kernel loads the host
+// partials and stores the host results itself, over the CPU-GPU link
+// (NVLink-C2C on GB300), with one persistent CTA per SM.
+int reduce_host_direct_locked(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem,
+                              int dst_dtype, int wire_dtype, cudaStream_t stream) {
+    const Context &c = g_ctx;
+    if (n_dsts < 1 || n_dsts > AR_MAX_DSTS) return AR_ERR_INVALID_ARG;
+    const void *s[AR_MAX_RANKS];
+    void *d[AR_MAX_DSTS];
+    for (int r = 0; r < c.R; ++r) {
+        if (!h_srcs[r] && nelem) return AR_ERR_INVALID_ARG;
+        s[r] = nelem ? device_view(h_srcs[r]) : h_srcs[r];
+        if (nelem && !s[r]) return AR_ERR_INVALID_ARG;
+    }
+    for (int k = 0; k < n_dsts; ++k) {
+        if (!h_dsts[k] && nelem) return AR_ERR_INVALID_ARG;
+        d[k] = nelem ? device_view(h_dsts[k]) : h_dsts[k];
+        if (nelem && !d[k]) return AR_ERR_INVALID_ARG;
+    }
+    const int st = ar_check_args(c.R, s, d, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+    if (st != AR_OK || nelem == 0) return st;
+    const bool vector_ok = [&] {
+        uintptr_t bits = 0;
+        for (int r = 0; r < c.R; ++r) bits |= reinterpret_cast<uintptr_t>(s[r]);
+        for (int k = 0; k < n_dsts; ++k) bits |= reinterpret_cast<uintptr_t>(d[k]);
+        return bits % 16 == 0;
+    }();
+    return launch_locked(s, d, n_dsts, nelem, dst_dtype, wire_dtype,
+                         vector_ok ? AR_VARIANT_BANDWIDTH : AR_VARIANT_AUTO, vector_ok ? c.sm_count : 0, stream,
+                         false);
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,6 +351,7 @@ int ar_init(int R, size_t max_elems) {
     if (variant < 0) return AR_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mu);
+    destroy_pipe(g_ctx.pipe);
     g_ctx = Context{};
     int dev = -1, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
@@ -289,6 +375,7 @@ int ar_init(int R, size_t max_elems) {
         if (end == s || v < 0) return AR_ERR_INVALID_ARG;
         c.latency_max_bytes = v;
     }
+    if (!create_pipe(c.pipe)) return AR_ERR_CUDA;
     c.ready = true;
     g_ctx = c;
     if (const char *s = getenv("AR_LOG"); s && !strcmp(s, "1")) {
@@ -300,6 +387,7 @@ int ar_init(int R, size_t max_elems) {
 
 void ar_free(void) {
     std::lock_guard<std::mutex> lock(g_mu);
+    destroy_pipe(g_ctx.pipe);
     g_ctx = Context{};
 }
 
@@ -334,6 +422,7 @@ int ar_query(int key, int64_t *value) {
         case AR_Q_LAST_VARIANT: *value = c.last_variant; break;
         case AR_Q_FAULT_INJECT: *value = c.fault_inject; break;
         case AR_Q_BW_BLOCKS_PER_SM: *value = c.bw_blocks_per_sm; break;
+        case AR_Q_HOST_CHUNK_BYTES: *value = c.host_chunk_bytes; break;
         default: return AR_ERR_INVALID_ARG;
     }
     return AR_OK;
@@ -357,6 +446,10 @@ int ar_set_option(int key, int64_t value) {
             if (value < 0 || value > 64) return AR_ERR_INVALID_ARG;
             c.bw_blocks_per_sm = static_cast<int>(value);
             break;
+        case AR_Q_HOST_CHUNK_BYTES:
+            if (value < 1) return AR_ERR_INVALID_ARG;
+            c.host_chunk_bytes = value;
+            break;
         default: return AR_ERR_INVALID_ARG;
     }
     return AR_OK;
@@ -368,8 +461,9 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
     if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
     const Context &c = g_ctx;
     if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
+    if (!d_srcs != !d_dsts) return AR_ERR_INVALID_ARG;
+    if (!d_srcs) return reduce_host_direct_locked(h_srcs, h_dsts, n_dsts, nelem, dst_dtype, wire_dtype, stream);
     const void *srcs_c[AR_MAX_RANKS];
-    if (!d_srcs || c.R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
     for (int r = 0; r < c.R; ++r) srcs_c[r] = d_srcs[r];
     const int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
     if (st != AR_OK) return st;
@@ -379,16 +473,46 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
     for (int d = 0; d < n_dsts; ++d)
         if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
     if (c.fault_inject) return AR_ERR_CUDA;
-    const size_t bytes = nelem * elem_bytes(dst_dtype);
-    for (int r = 0; r < c.R; ++r)
-        if (cudaMemcpyAsync(d_srcs[r], h_srcs[r], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+
+    // Chunks of whole 256-element groups (so every chunk keeps the buffers'
+    // alignment); chunking never changes a result bit.
+    const size_t esize = elem_bytes(dst_dtype);
+    size_t chunk = static_cast<size_t>(c.host_chunk_bytes) / esize;
+    const size_t min_chunk = (nelem + kMaxHostChunks - 1) / kMaxHostChunks;
+    if (chunk < min_chunk) chunk = min_chunk;
+    chunk = (chunk + 255) / 256 * 256;
+    const HostPipe &pp = c.pipe;
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // everything the caller enqueued on `stream` before this call comes first
+    if (!ok(cudaEventRecord(pp.start, stream)) || !ok(cudaStreamWaitEvent(pp.h2d, pp.start, 0)) ||
+        !ok(cudaStreamWaitEvent(pp.comp, pp.start, 0)) || !ok(cudaStreamWaitEvent(pp.d2h, pp.start, 0)))
+        return AR_ERR_CUDA;
+    const void *cs[AR_MAX_RANKS];
+    void *cd[AR_MAX_DSTS];
+    int k = 0;
+    for (size_t off = 0; off < nelem; off += chunk, ++k) {
+        const size_t n = nelem - off < chunk ? nelem - off : chunk;
+        const size_t boff = off * esize, nb = n * esize;
+        for (int r = 0; r < c.R; ++r) {
+            char *dptr = static_cast<char *>(d_srcs[r]) + boff;
+            if (!ok(cudaMemcpyAsync(dptr, static_cast<const char *>(h_srcs[r]) + boff, nb, cudaMemcpyHostToDevice,
+                                    pp.h2d)))
+                return AR_ERR_CUDA;
+            cs[r] = dptr;
+        }
+        for (int d = 0; d < n_dsts; ++d) cd[d] = static_cast<char *>(d_dsts[d]) + boff;
+        if (!ok(cudaEventRecord(pp.copied[k], pp.h2d)) || !ok(cudaStreamWaitEvent(pp.comp, pp.copied[k], 0)))
             return AR_ERR_CUDA;
-    const int lst = launch_locked(srcs_c, d_dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, stream,
-                                  false);
-    if (lst != AR_OK) return lst;
-    for (int d = 0; d < n_dsts; ++d)
-        if (cudaMemcpyAsync(h_dsts[d], d_dsts[d], bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        const int lst = launch_locked(cs, cd, n_dsts, n, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, pp.comp, false);
+        if (lst != AR_OK) return lst;
+        if (!ok(cudaEventRecord(pp.reduced[k], pp.comp)) || !ok(cudaStreamWaitEvent(pp.d2h, pp.reduced[k], 0)))
             return AR_ERR_CUDA;
+        for (int d = 0; d < n_dsts; ++d)
+            if (!ok(cudaMemcpyAsync(static_cast<char *>(h_dsts[d]) + boff, cd[d], nb, cudaMemcpyDeviceToHost, pp.d2h)))
+                return AR_ERR_CUDA;
+    }
+    // the caller's stream continues once the last copy back has finished
+    if (!ok(cudaEventRecord(pp.done, pp.d2h)) || !ok(cudaStreamWaitEvent(stream, pp.done, 0))) return AR_ERR_CUDA;
     return AR_OK;
 }
 

@@ -259,3 +259,93 @@ def test_persistent_grid_option(ctx, per_sm, dst, R):
         tps.ar_set_option("bw_blocks_per_sm", 0)
     for o in outs:
         assert_same(o, exp, dst, f"persistent per_sm={per_sm}")
+
+
+@pytest.mark.parametrize("chunk_bytes", [4096, 65536, 1 << 22])
+@pytest.mark.parametrize("dst,wire,n", [("f32", "bf16", 1_000_003), ("bf16", "bf16", 777_777), ("f32", "f16", 4099)])
+def test_host_entry_chunked_pipeline(ctx, chunk_bytes, dst, wire, n):
+    """ar_reduce_host in chunks over its own streams: same bits as the
+    oracle for every chunk size (small chunks hit the 64-chunk cap), on a
+    non-default caller stream, twice in a row on the same staging buffers."""
+    R, n_dsts = 3, 2
+    ctx.ensure(R, n)
+    tps.ar_set_option("host_chunk_bytes", chunk_bytes)
+    try:
+        stream = torch.cuda.Stream()
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dst]
+        d_srcs = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(R)]
+        d_dsts = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(n_dsts)]
+        for call in range(2):
+            srcs = srcs_for(chunk_bytes + call, R, n, dst)
+            exp = expect(srcs, dst, wire)
+            h_srcs = [torch.from_numpy(s.view(np.int16) if s.dtype == np.uint16 else s).pin_memory() for s in srcs]
+            h_dsts = [torch.empty(n, dtype=h_srcs[0].dtype).pin_memory() for _ in range(n_dsts)]
+            tps.ar_reduce_host(h_srcs, h_dsts, d_srcs, d_dsts, nelem=n, dst_dtype=dst, wire_dtype=wire, stream=stream)
+            stream.synchronize()
+            for h in h_dsts:
+                assert_same(h.numpy().view(np.uint32 if dst == "f32" else np.uint16), exp, dst,
+                            f"host pipeline chunk={chunk_bytes} call={call}")
+    finally:
+        tps.ar_set_option("host_chunk_bytes", 4 << 20)
+
+
+def test_host_entry_in_place(ctx):
+    """Device staging destination equal to a device staging source."""
+    R, n = 2, 300_001
+    ctx.ensure(R, n)
+    srcs = srcs_for(99, R, n, "f32")
+    exp = expect(srcs, "f32", "bf16")
+    h_srcs = [torch.from_numpy(s).pin_memory() for s in srcs]
+    h_dst = torch.empty(n, dtype=torch.float32).pin_memory()
+    d_srcs = [torch.empty(n, device="cuda") for _ in range(R)]
+    tps.ar_set_option("host_chunk_bytes", 65536)
+    try:
+        tps.ar_reduce_host(h_srcs, [h_dst], d_srcs, [d_srcs[1]], nelem=n, dst_dtype="f32", wire_dtype="bf16")
+        torch.cuda.synchronize()
+    finally:
+        tps.ar_set_option("host_chunk_bytes", 4 << 20)
+    assert_same(h_dst.numpy(), exp, "f32", "host in place")
+    assert_same(to_host(d_srcs[1], "f32"), exp, "f32", "device destination")
+
+
+@pytest.mark.parametrize("dst,wire,R,n", [("f32", "bf16", 2, 1_000_003), ("bf16", "bf16", 4, 333_333),
+                                          ("f32", "f16", 8, 4099)])
+def test_host_entry_direct(ctx, dst, wire, R, n):
+    """ar_reduce_host without staging buffers: the kernel reads the pinned
+    host partials and writes the pinned host results itself."""
+    ctx.ensure(R, n)
+    srcs = srcs_for(R * 13 + n, R, n, dst)
+    exp = expect(srcs, dst, wire)
+    h_srcs = [torch.from_numpy(s.view(np.int16) if s.dtype == np.uint16 else s).pin_memory() for s in srcs]
+    h_dsts = [torch.empty(n, dtype=h_srcs[0].dtype).pin_memory() for _ in range(2)]
+    stream = torch.cuda.Stream()
+    tps.ar_reduce_host(h_srcs, h_dsts, nelem=n, dst_dtype=dst, wire_dtype=wire, stream=stream)
+    stream.synchronize()
+    for h in h_dsts:
+        assert_same(h.numpy().view(np.uint32 if dst == "f32" else np.uint16), exp, dst, "direct host")
+
+
+def test_host_entry_direct_unaligned_and_in_place(ctx):
+    R, n = 3, 50_001
+    ctx.ensure(R, n)
+    srcs = srcs_for(5150, R, n, "f32")
+    exp = expect(srcs, "f32", "f16")
+    backs = [torch.empty(n + 1, dtype=torch.float32).pin_memory() for _ in range(R)]
+    h_srcs = [b[1:] for b in backs]  # 4 bytes off 16-byte alignment
+    for h, s in zip(h_srcs, srcs):
+        h.copy_(torch.from_numpy(s))
+    tps.ar_reduce_host(h_srcs, [h_srcs[2]], nelem=n, dst_dtype="f32", wire_dtype="f16")
+    torch.cuda.synchronize()
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS["scalar"]
+    assert_same(h_srcs[2].numpy(), exp, "f32", "direct, unaligned, in place")
+
+
+def test_host_entry_direct_rejects_pageable_memory(ctx):
+    ctx.ensure(2, 1024)
+    a = np.ones(1024, dtype=np.float32)
+    b = np.ones(1024, dtype=np.float32)
+    out = np.full(1024, 7.0, dtype=np.float32)
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce_host([a, b], [out], nelem=1024, dst_dtype="f32", wire_dtype="bf16")
+    assert e.value.status == 1
+    assert (out == 7.0).all()
