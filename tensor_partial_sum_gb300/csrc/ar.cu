@@ -196,12 +196,14 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     const long long sms = c.sm_count;
     KernelFn fn = nullptr;
     int threads = 0, grid = 0;
+    int plan_vec_bytes = 0;  // vector width of an ar_reduce_kernel launch, 0 for the other kernels
     switch (variant) {
         case AR_VARIANT_LATENCY: {
             // 16-byte vectors, one per thread, a grid that covers the tensor
             const tps::VecKernels &vk = k.v16;
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kLatencyThreads;
+            plan_vec_bytes = 16;
             const long long nv = static_cast<long long>(nelem / (16 / esize));
             grid = grid_cap((nv + threads - 1) / threads, 0x7FFFFFFFll);
             break;
@@ -214,6 +216,7 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             const int vec_bytes = wide ? k.wide_bytes : 16;
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kBandwidthThreads;
+            plan_vec_bytes = vec_bytes;
             const long long nv = static_cast<long long>(nelem / (vec_bytes / esize));
             const long long full = (nv + threads - 1) / threads;
             if (grid_blocks > 0) {
@@ -243,6 +246,13 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         default: return AR_ERR_INVALID_ARG;
     }
 
+    if (plan_vec_bytes > 0) {
+        // rounds and chunk of ar_reduce_kernel for this grid (one vector per thread per round)
+        const unsigned long long nv = nelem / (plan_vec_bytes / esize);
+        const unsigned long long per_round = static_cast<unsigned long long>(grid) * threads;
+        p.rounds = (nv + per_round - 1) / per_round;
+        p.chunk = p.rounds ? (nv + p.rounds * grid - 1) / (p.rounds * grid) : 0;
+    }
     fn<<<grid, threads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
     c.last_variant = variant;

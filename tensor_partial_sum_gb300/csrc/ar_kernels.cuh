@@ -30,6 +30,10 @@ struct ArParams {
     const void *src[kMaxRanks];
     void *dst[kMaxDsts];
     unsigned long long nelem;
+    // Work plan of ar_reduce_kernel, computed by the host for the launch's
+    // grid: `rounds` rounds of `chunk` vectors per CTA (see the kernel).
+    unsigned long long chunk;
+    unsigned long long rounds;
     int R;
     int n_dsts;
 };
@@ -309,12 +313,11 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
     const size_t nvec = p.nelem / V;
     const size_t G = gridDim.x;
     const size_t b = blockIdx.x;
-    const size_t tile = static_cast<size_t>(blockDim.x) * U;
     pdl_launch_dependents();
     pdl_wait();
-    if (nvec > 0) {
-        const size_t K = (nvec + G * tile - 1) / (G * tile);
-        const size_t c = (nvec + K * G - 1) / (K * G);
+    {
+        const size_t K = p.rounds;  // ceil(nvec / (G * blockDim.x * U)), from the host
+        const size_t c = p.chunk;   // ceil(nvec / (K * G)), from the host
         for (size_t k = 0; k < K; ++k) {
             const size_t first = (k * G + b) * c;
             if (first >= nvec) break;
