@@ -98,6 +98,11 @@ class Oracle:
         L.orc_reduce_range.restype = i
         L.orc_reduce.argtypes = [i, vp, vp, i, sz, i, i]
         L.orc_reduce.restype = i
+        ll_p = ctypes.POINTER(ctypes.c_longlong)
+        L.orc_reduce_2d.argtypes = [i, vp, ll_p, ctypes.c_uint, vp, ctypes.c_longlong, vp, ll_p, i, sz, sz, i, i]
+        L.orc_reduce_2d.restype = i
+        L.orc_wire_pack.argtypes = [vp, vp, sz, i, i]
+        L.orc_wire_pack.restype = i
         self.lib = L
         self.path = path
 
@@ -138,6 +143,48 @@ class Oracle:
         return out
 
 
+    def reduce_2d(self, srcs, n_dsts, dst_dtype, wire_dtype, ne0, ne1, src_strides=None, dst_strides=None,
+                  inactive=(), residual=None, residual_stride=None, out=None):
+        """2-D reduction with row strides (bytes), inactive ranks (+0
+        operands; their source may be None), and an optional residual
+        (``residual_stride`` 0 = one row broadcast to every row).  Sources
+        and outputs are flat storage arrays holding the strided rows."""
+        es = 4 if dst_dtype == "f32" else 2
+        srcs = [None if s is None else _as_storage(s, dst_dtype).ravel() for s in srcs]
+        mask = 0
+        for r in inactive:
+            mask |= 1 << r
+        if out is None:
+            ds = dst_strides or [ne0 * es] * n_dsts
+            out = [np.zeros(max(1, ((ne1 - 1) * ds[d] + ne0 * es) // es) if ne1 else 1, dtype=_STORAGE[dst_dtype])
+                   for d in range(n_dsts)]
+        else:
+            out = [_as_storage(o, dst_dtype).reshape(-1) for o in out]
+        src_arr = (ctypes.c_void_p * len(srcs))(*[None if s is None else s.ctypes.data for s in srcs])
+        ll = ctypes.c_longlong
+        ss = None if src_strides is None else (ll * len(src_strides))(*src_strides)
+        dd = None if dst_strides is None else (ll * len(dst_strides))(*dst_strides)
+        res = None
+        if residual is not None:
+            residual = _as_storage(residual, dst_dtype).ravel()
+            res = residual.ctypes.data
+            if residual_stride is None:
+                residual_stride = ne0 * es
+        rc = self.lib.orc_reduce_2d(len(srcs), src_arr, ss, mask, res, residual_stride or 0, _ptr_array(out), dd,
+                                    n_dsts, ne0, ne1, DTYPES[dst_dtype], DTYPES[wire_dtype])
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return out
+
+    def wire_pack(self, src, dst_dtype, wire_dtype):
+        src = _as_storage(src, dst_dtype).ravel()
+        out = np.empty(src.size, dtype=_STORAGE[wire_dtype])
+        if self.lib.orc_wire_pack(src.ctypes.data, out.ctypes.data, src.size, DTYPES[dst_dtype],
+                                  DTYPES[wire_dtype]) != 0:
+            raise ValueError("oracle rejected the arguments")
+        return out
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -160,3 +207,11 @@ def round_to(name, x):
 
 def reduce(srcs, n_dsts, dst_dtype, wire_dtype, begin=0, end=None, out=None):
     return default().reduce(srcs, n_dsts, dst_dtype, wire_dtype, begin, end, out)
+
+
+def reduce_2d(*args, **kwargs):
+    return default().reduce_2d(*args, **kwargs)
+
+
+def wire_pack(src, dst_dtype, wire_dtype):
+    return default().wire_pack(src, dst_dtype, wire_dtype)

@@ -209,3 +209,59 @@ int orc_reduce(int R, const void *const *srcs, void *const *dsts, int n_dsts,
                size_t nelem, int dst_dtype, int wire_dtype) {
     return orc_reduce_range(R, srcs, dsts, n_dsts, 0, nelem, dst_dtype, wire_dtype);
 }
+
+/* Element i of a row that starts at byte offset row_off of base. */
+static uint32_t load_bits_at(int dtype, const void *base, long long row_off, size_t i) {
+    return load_bits(dtype, (const char *)base + row_off, i);
+}
+
+int orc_reduce_2d(int R, const void *const *srcs, const long long *src_strides, unsigned inactive_mask,
+                  const void *residual, long long residual_stride, void *const *dsts,
+                  const long long *dst_strides, int n_dsts, size_t ne0, size_t ne1, int dst_dtype,
+                  int wire_dtype) {
+    const size_t es = orc_elem_size(dst_dtype);
+    if (R < 1 || R > 32 || n_dsts < 1 || !srcs || !dsts) return -1;
+    if (!es || !orc_elem_size(wire_dtype)) return -1;
+    for (int r = 0; r < R; ++r)
+        if (!srcs[r] && !((inactive_mask >> r) & 1u)) return -1;
+    for (int d = 0; d < n_dsts; ++d)
+        if (!dsts[d]) return -1;
+    const long long packed = (long long)(ne0 * es);
+
+    for (size_t j = 0; j < ne1; ++j) {
+        for (size_t i = 0; i < ne0; ++i) {
+            float acc = 0.0f;
+            for (int r = 0; r < R; ++r) {
+                float w;
+                if ((inactive_mask >> r) & 1u) {
+                    /* an inactive rank's data are zeros: its operand is +0 */
+                    w = orc_widen(wire_dtype, orc_round(wire_dtype, 0.0f));
+                } else {
+                    const long long stride = src_strides ? src_strides[r] : packed;
+                    const float v = orc_widen(dst_dtype, load_bits_at(dst_dtype, srcs[r], (long long)j * stride, i));
+                    w = orc_widen(wire_dtype, orc_round(wire_dtype, v));
+                }
+                acc = (r == 0) ? w : acc + w;
+            }
+            if (residual) {
+                const long long off = (long long)j * residual_stride;
+                acc = acc + orc_widen(dst_dtype, load_bits_at(dst_dtype, residual, off, i));
+            }
+            const uint32_t y = orc_round(dst_dtype, acc);
+            for (int d = 0; d < n_dsts; ++d) {
+                const long long stride = dst_strides ? dst_strides[d] : packed;
+                store_bits(dst_dtype, (char *)dsts[d] + (long long)j * stride, i, y);
+            }
+        }
+    }
+    return 0;
+}
+
+int orc_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype) {
+    if (!src || !wire || !orc_elem_size(dst_dtype) || !orc_elem_size(wire_dtype)) return -1;
+    for (size_t i = 0; i < nelem; ++i) {
+        const float v = orc_widen(dst_dtype, load_bits(dst_dtype, src, i));
+        store_bits(wire_dtype, wire, i, orc_round(wire_dtype, v));
+    }
+    return 0;
+}

@@ -77,6 +77,39 @@ int orc_reduce_range(int R, const void *const *srcs, void *const *dsts, int n_ds
 int orc_reduce(int R, const void *const *srcs, void *const *dsts, int n_dsts,
                size_t nelem, int dst_dtype, int wire_dtype);
 
+/*
+ * The reduction over a 2-D tensor of ne1 rows of ne0 elements, with the
+ * three extensions the pages describe around the same fold:
+ *   - row strides in bytes for every source and destination (NULL: rows
+ *     packed), as the 2-D DMA variant of ggml-hexagon allreduce-ops.c
+ *     (DEFINE_ALLREDUCE_THREAD_DMA_2D) walks rows through nb[1];
+ *   - inactive ranks: bit r of inactive_mask set means rank r contributes
+ *     +0 for every element (its source may be NULL), as
+ *     ggml_cuda_ar_allreduce in ggml-cuda allreduce.cu zeroes the data of
+ *     shards without the compute flag before reducing;
+ *   - a residual in T_dst added after the rank fold and before the final
+ *     cast (the ALLREDUCE_ADD variants of allreduce-ops.c add the residual
+ *     after the ranks); residual_stride is its row stride in bytes, 0 means
+ *     one row broadcast to every row (the row-broadcast "add_bcast"
+ *     variant).  The residual does not cross the wire, so it is not rounded
+ *     through the wire type; it is added in float.
+ * Per element (row j, column i):
+ *     acc = w_0; acc = acc + w_r for r = 1..R-1   (w_r = +0 for an inactive rank)
+ *     if residual: acc = acc + value(residual[j][i])
+ *     dst[d][j][i] = round<T_dst>(acc)
+ */
+int orc_reduce_2d(int R, const void *const *srcs, const long long *src_strides, unsigned inactive_mask,
+                  const void *residual, long long residual_stride, void *const *dsts,
+                  const long long *dst_strides, int n_dsts, size_t ne0, size_t ne1, int dst_dtype,
+                  int wire_dtype);
+
+/*
+ * The wire cast materialised: wire[i] = round<T_wire>(value(src[i])), the
+ * buffer phase 1 of ggml_cuda_ar_kernel (ggml-cuda allreduce.cu) writes
+ * before sending it to the peer.
+ */
+int orc_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype);
+
 #ifdef __cplusplus
 }
 #endif
