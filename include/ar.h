@@ -203,6 +203,73 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
                    int dst_dtype, int wire_dtype, void *const *d_srcs, void *const *d_dsts,
                    cudaStream_t stream);
 
+/*
+ * Layout of an extended reduction (ar_reduce_ex): a 2-D tensor of ne1 rows
+ * of ne0 elements with per-buffer row strides, ranks that may be inactive,
+ * and an optional residual or bias added after the rank fold.
+ *
+ * Where this comes from:
+ *   - row strides: the 2-D DMA variant DEFINE_ALLREDUCE_THREAD_DMA_2D of
+ *     ggml-hexagon htp/allreduce-ops.c walks every source and destination
+ *     row by row through its nb[1] byte stride;
+ *   - residual and bias: the ALLREDUCE_ADD variants of the same file add one
+ *     more tensor after the ranks (add_bcast adds one row to every row);
+ *   - inactive ranks: ggml_cuda_ar_allreduce in ggml-cuda allreduce.cu zeroes
+ *     the data of shards that did not compute, so they contribute zeros.
+ * Readings taken where the pages are silent: the residual is added in float
+ * after the rank fold and before the one final cast, and is not rounded
+ * through the wire type (it never crosses the wire); an inactive rank
+ * contributes +0 to every element, which is not the same as leaving it out
+ * (-0 + +0 = +0).
+ */
+typedef struct {
+    size_t ne0;                   /* elements per row */
+    size_t ne1;                   /* rows; ne0 * ne1 <= max_elems */
+    const int64_t *src_row_bytes; /* R row strides in bytes (>= ne0 * element size, a multiple of
+                                     the element size), or NULL: every source's rows are packed */
+    const int64_t *dst_row_bytes; /* n_dsts row strides in bytes, or NULL: packed */
+    const void *residual;         /* NULL, or a T_dst tensor added after the rank fold */
+    int64_t residual_row_bytes;   /* residual row stride in bytes; 0: the residual is one row of
+                                     ne0 elements added to every row (a bias) */
+    uint32_t inactive_mask;       /* bit r set: rank r contributes +0 everywhere and srcs[r] is not
+                                     read (it may be NULL); bits >= R must be clear */
+} ar_layout;
+
+/*
+ * ar_reduce_ex -- the reduction over an ar_layout, enqueued on `stream`:
+ *   dst[d][row][i] = T_dst( fold_r wire(src[r][row][i]) (+ residual[row][i]) )
+ * with the fold, casts and rounding of ar_reduce.  srcs has R entries (NULL
+ * allowed for inactive ranks), dsts has n_dsts.  A destination may be
+ * exactly a source or exactly the residual (same pointer and same row
+ * stride: an in-place update such as x = x + allreduce(partials)); any other
+ * overlap of the buffers' row spans is AR_ERR_OVERLAP (the check is
+ * conservative: interleaved rows that never touch are also refused).
+ * 16-byte-aligned buffers and strides take the vector path; any other
+ * element-aligned layout works element by element with the same bits.
+ * Statuses as for ar_reduce; nothing is enqueued unless AR_OK.
+ */
+int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const ar_layout *layout,
+                 int dst_dtype, int wire_dtype, cudaStream_t stream);
+
+/* Host-only validation of an ar_reduce_ex call on explicit R and max_elems
+ * (no CUDA call; runs without a GPU). */
+int ar_check_layout(int R, const void *const *srcs, void *const *dsts, int n_dsts, const ar_layout *layout,
+                    size_t max_elems, int dst_dtype, int wire_dtype);
+
+/*
+ * ar_wire_pack -- materialise the wire copy of one partial:
+ *   wire[i] = T_wire(src[i]) for i < nelem,
+ * the buffer a transport sends to the other ranks (phase 1 of
+ * ggml_cuda_ar_kernel in ggml-cuda allreduce.cu writes exactly this; its
+ * copy-engine path converts to bf16 into a temporary before copying).
+ *   src   nelem elements of dst_dtype (device-accessible).
+ *   wire  nelem elements of wire_dtype; may be src itself when both types
+ *         have the same size, otherwise must not overlap it.
+ * Needs ar_init (nelem <= max_elems).  Statuses as for ar_reduce.
+ */
+int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype,
+                 cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

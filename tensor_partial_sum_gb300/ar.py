@@ -27,6 +27,15 @@ KEYS = {"ranks": 0, "max_elems": 1, "device": 2, "sm_count": 3, "latency_max_byt
 _lib = None
 
 
+class ArLayout(ctypes.Structure):
+    """ar_layout of include/ar.h."""
+    _fields_ = [("ne0", ctypes.c_size_t), ("ne1", ctypes.c_size_t),
+                ("src_row_bytes", ctypes.POINTER(ctypes.c_int64)),
+                ("dst_row_bytes", ctypes.POINTER(ctypes.c_int64)),
+                ("residual", ctypes.c_void_p), ("residual_row_bytes", ctypes.c_int64),
+                ("inactive_mask", ctypes.c_uint32)]
+
+
 class ARError(RuntimeError):
     def __init__(self, status: int, call: str):
         self.status = status
@@ -63,6 +72,13 @@ def lib() -> ctypes.CDLL:
         L.ar_set_option.restype = i
         L.ar_reduce_host.argtypes = [pp, pp, i, sz, i, i, pp, pp, vp]
         L.ar_reduce_host.restype = i
+        lp = ctypes.POINTER(ArLayout)
+        L.ar_reduce_ex.argtypes = [pp, pp, i, lp, i, i, vp]
+        L.ar_reduce_ex.restype = i
+        L.ar_check_layout.argtypes = [i, pp, pp, i, lp, sz, i, i]
+        L.ar_check_layout.restype = i
+        L.ar_wire_pack.argtypes = [vp, vp, sz, i, i, vp]
+        L.ar_wire_pack.restype = i
         _lib = L
     return _lib
 
@@ -185,3 +201,49 @@ def ar_reduce_host(h_srcs, h_dsts, d_srcs=None, d_dsts=None, nelem=None, dst_dty
     nelem, dcode = _infer(d_srcs if d_srcs is not None else h_srcs, nelem, dst_dtype)
     _check(lib().ar_reduce_host(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode, _dtype_code(wire_dtype),
                                 _ptrs(d_srcs), _ptrs(d_dsts), _stream(stream)), "ar_reduce_host")
+
+
+def make_layout(ne0, ne1, src_row_bytes=None, dst_row_bytes=None, residual=None, residual_row_bytes=None,
+                inactive=()) -> ArLayout:
+    """An ar_layout.  With a residual, ``residual_row_bytes`` is its row
+    stride in bytes (0: one bias row broadcast to every row; None: packed
+    rows, which needs a tensor residual to know the element size);
+    ``inactive`` lists rank indices."""
+    L = ArLayout()
+    L.ne0, L.ne1 = ne0, ne1
+    if src_row_bytes is not None:
+        L.src_row_bytes = (ctypes.c_int64 * len(src_row_bytes))(*src_row_bytes)
+    if dst_row_bytes is not None:
+        L.dst_row_bytes = (ctypes.c_int64 * len(dst_row_bytes))(*dst_row_bytes)
+    L.residual = _ptr(residual)
+    if residual is not None and residual_row_bytes is None:
+        residual_row_bytes = ne0 * residual.element_size()
+    L.residual_row_bytes = residual_row_bytes or 0
+    mask = 0
+    for r in inactive:
+        mask |= 1 << r
+    L.inactive_mask = mask
+    return L
+
+
+def ar_reduce_ex(srcs, dsts, layout: ArLayout, dst_dtype, wire_dtype="bf16", stream=None) -> None:
+    """Reduction over an ar_layout (row strides, inactive ranks as None
+    sources, residual or bias)."""
+    _check(lib().ar_reduce_ex(_ptrs(srcs), _ptrs(dsts), len(dsts), ctypes.byref(layout), _dtype_code(dst_dtype),
+                              _dtype_code(wire_dtype), _stream(stream)), "ar_reduce_ex")
+
+
+def ar_check_layout(R, srcs, dsts, layout: ArLayout, max_elems, dst_dtype, wire_dtype) -> int:
+    """Host-only validation of an ar_reduce_ex call; returns the status."""
+    return lib().ar_check_layout(R, _ptrs(srcs), _ptrs(dsts), len(dsts), ctypes.byref(layout), max_elems,
+                                 _dtype_code(dst_dtype), _dtype_code(wire_dtype))
+
+
+def ar_wire_pack(src, wire, nelem=None, dst_dtype=None, wire_dtype="bf16", stream=None) -> None:
+    """wire[i] = T_wire(src[i]): the wire copy a transport would send."""
+    if nelem is None:
+        nelem = src.numel()
+    if dst_dtype is None:
+        dst_dtype = src.dtype
+    _check(lib().ar_wire_pack(_ptr(src), _ptr(wire), nelem, _dtype_code(dst_dtype), _dtype_code(wire_dtype),
+                              _stream(stream)), "ar_wire_pack")

@@ -526,4 +526,175 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
     return AR_OK;
 }
 
+// ---- extended layouts --------------------------------------------------------
+
+namespace {
+
+// Byte span [start, end) a buffer of ne1 rows at `stride` touches.
+struct Span {
+    uintptr_t start, end;
+    int64_t stride;
+};
+
+bool make_span(const void *p, int64_t stride, size_t ne0, size_t ne1, size_t es, Span *out) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const unsigned __int128 len = static_cast<unsigned __int128>(ne1 - 1) * static_cast<uint64_t>(stride) +
+                                  static_cast<unsigned __int128>(ne0) * es;
+    if (len > static_cast<unsigned __int128>(UINTPTR_MAX - a)) return false;
+    *out = Span{a, a + static_cast<uintptr_t>(len), stride};
+    return true;
+}
+
+bool spans_overlap(const Span &x, const Span &y) { return x.start < y.end && y.start < x.end; }
+
+bool valid_stride(int64_t stride, size_t ne0, size_t es) {
+    return stride >= 0 && static_cast<uint64_t>(stride) >= ne0 * es && stride % static_cast<int64_t>(es) == 0;
+}
+
+}  // namespace
+
+int ar_check_layout(int R, const void *const *srcs, void *const *dsts, int n_dsts, const ar_layout *L,
+                    size_t max_elems, int dst_dtype, int wire_dtype) {
+    if (R < 1 || R > AR_MAX_RANKS || n_dsts < 1 || n_dsts > AR_MAX_DSTS) return AR_ERR_INVALID_ARG;
+    if (!srcs || !dsts || !L) return AR_ERR_INVALID_ARG;
+    const size_t es = elem_bytes(dst_dtype);
+    if (!es || !elem_bytes(wire_dtype)) return AR_ERR_UNSUPPORTED;
+    if (R < 32 && (L->inactive_mask >> R) != 0) return AR_ERR_INVALID_ARG;
+    if (L->ne0 && L->ne1 > SIZE_MAX / L->ne0) return AR_ERR_TOO_LARGE;
+    const size_t nelem = L->ne0 * L->ne1;
+    if (nelem > max_elems) return AR_ERR_TOO_LARGE;
+    if (nelem == 0) return AR_OK;
+    const int64_t packed = static_cast<int64_t>(L->ne0 * es);
+    Span dsp[AR_MAX_DSTS], ssp[AR_MAX_RANKS], rsp{};
+    bool active[AR_MAX_RANKS];
+    for (int r = 0; r < R; ++r) {
+        active[r] = !((L->inactive_mask >> r) & 1u);
+        if (!active[r]) continue;
+        const int64_t st = L->src_row_bytes ? L->src_row_bytes[r] : packed;
+        if (!srcs[r] || reinterpret_cast<uintptr_t>(srcs[r]) % es) return AR_ERR_INVALID_ARG;
+        if (L->ne1 > 1 && !valid_stride(st, L->ne0, es)) return AR_ERR_INVALID_ARG;
+        if (!make_span(srcs[r], L->ne1 > 1 ? st : packed, L->ne0, L->ne1, es, &ssp[r])) return AR_ERR_INVALID_ARG;
+    }
+    for (int d = 0; d < n_dsts; ++d) {
+        const int64_t st = L->dst_row_bytes ? L->dst_row_bytes[d] : packed;
+        if (!dsts[d] || reinterpret_cast<uintptr_t>(dsts[d]) % es) return AR_ERR_INVALID_ARG;
+        if (L->ne1 > 1 && !valid_stride(st, L->ne0, es)) return AR_ERR_INVALID_ARG;
+        if (!make_span(dsts[d], L->ne1 > 1 ? st : packed, L->ne0, L->ne1, es, &dsp[d])) return AR_ERR_INVALID_ARG;
+    }
+    const bool bcast = L->residual && L->residual_row_bytes == 0;
+    if (L->residual) {
+        if (reinterpret_cast<uintptr_t>(L->residual) % es) return AR_ERR_INVALID_ARG;
+        if (!bcast && L->ne1 > 1 && !valid_stride(L->residual_row_bytes, L->ne0, es)) return AR_ERR_INVALID_ARG;
+        const int64_t st = (bcast || L->ne1 <= 1) ? packed : L->residual_row_bytes;
+        if (!make_span(L->residual, st, L->ne0, bcast ? 1 : L->ne1, es, &rsp)) return AR_ERR_INVALID_ARG;
+    }
+    for (int d = 0; d < n_dsts; ++d) {
+        for (int r = 0; r < R; ++r) {
+            if (!active[r] || !spans_overlap(dsp[d], ssp[r])) continue;
+            const bool same = dsp[d].start == ssp[r].start && (L->ne1 <= 1 || dsp[d].stride == ssp[r].stride);
+            if (!same) return AR_ERR_OVERLAP;
+        }
+        if (L->residual && spans_overlap(dsp[d], rsp)) {
+            const bool same = !bcast && dsp[d].start == rsp.start && (L->ne1 <= 1 || dsp[d].stride == rsp.stride);
+            if (!same) return AR_ERR_OVERLAP;
+        }
+        for (int e = 0; e < d; ++e)
+            if (spans_overlap(dsp[d], dsp[e])) return AR_ERR_OVERLAP;
+    }
+    return AR_OK;
+}
+
+int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const ar_layout *L, int dst_dtype,
+                 int wire_dtype, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    Context &c = g_ctx;
+    const int st = ar_check_layout(c.R, srcs, dsts, n_dsts, L, c.max_elems, dst_dtype, wire_dtype);
+    if (st != AR_OK || L->ne0 * L->ne1 == 0) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (dev != c.device) return AR_ERR_INVALID_ARG;
+    if (c.fault_inject) return AR_ERR_CUDA;
+
+    const size_t es = elem_bytes(dst_dtype);
+    const int64_t packed = static_cast<int64_t>(L->ne0 * es);
+    tps::ArExParams p;
+    memset(&p, 0, sizeof p);
+    p.ne0 = L->ne0;
+    p.ne1 = L->ne1;
+    p.R = c.R;
+    p.n_dsts = n_dsts;
+    p.inactive = L->inactive_mask;
+    uintptr_t bits = 0;  // OR of every address and stride: its low bits give the common alignment
+    for (int r = 0; r < c.R; ++r) {
+        if ((L->inactive_mask >> r) & 1u) continue;
+        p.src[r] = srcs[r];
+        p.src_stride[r] = L->src_row_bytes ? L->src_row_bytes[r] : packed;
+        bits |= reinterpret_cast<uintptr_t>(srcs[r]) | (L->ne1 > 1 ? static_cast<uintptr_t>(p.src_stride[r]) : 0);
+    }
+    for (int d = 0; d < n_dsts; ++d) {
+        p.dst[d] = dsts[d];
+        p.dst_stride[d] = L->dst_row_bytes ? L->dst_row_bytes[d] : packed;
+        bits |= reinterpret_cast<uintptr_t>(dsts[d]) | (L->ne1 > 1 ? static_cast<uintptr_t>(p.dst_stride[d]) : 0);
+    }
+    if (L->residual) {
+        p.residual = L->residual;
+        p.res_stride = L->residual_row_bytes;
+        bits |= reinterpret_cast<uintptr_t>(L->residual) |
+                (L->ne1 > 1 ? static_cast<uintptr_t>(L->residual_row_bytes) : 0);
+    }
+    const bool vec = bits % 16 == 0;
+    const tps::Kernels &k = kernels_for(dst_dtype, wire_dtype);
+    const tps::ExKernelFn fn = k.ex[c.R > 2][L->residual != nullptr][vec];
+    const size_t V = 16 / es;
+    int threads = 256;
+    long long gx;
+    if (vec) {
+        const long long vpr = static_cast<long long>(L->ne0 / V);
+        if (vpr < 256) threads = static_cast<int>(vpr < 32 ? 32 : (vpr + 31) / 32 * 32);
+        gx = (vpr + threads - 1) / threads;
+    } else {
+        gx = (static_cast<long long>(L->ne0) + threads - 1) / threads;
+        if (gx > 1024) gx = 1024;
+    }
+    if (gx < 1) gx = 1;
+    const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
+    fn<<<dim3(static_cast<unsigned>(gx), gy), threads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    return AR_OK;
+}
+
+int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    const Context &c = g_ctx;
+    const size_t es = elem_bytes(dst_dtype), ew = elem_bytes(wire_dtype);
+    if (!es || !ew) return AR_ERR_UNSUPPORTED;
+    if (nelem > c.max_elems) return AR_ERR_TOO_LARGE;
+    if (nelem == 0) return AR_OK;
+    if (!src || !wire) return AR_ERR_INVALID_ARG;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(wire);
+    if (a % es || b % ew) return AR_ERR_INVALID_ARG;
+    if (a < b + nelem * ew && b < a + nelem * es && !(a == b && es == ew)) return AR_ERR_OVERLAP;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (dev != c.device) return AR_ERR_INVALID_ARG;
+    if (c.fault_inject) return AR_ERR_CUDA;
+    const size_t V = 16 / es;
+    const size_t out_bytes = V * ew;  // wire bytes per 16-byte source vector
+    const bool vec = a % 16 == 0 && b % (out_bytes > 16 ? out_bytes : 16) == 0;
+    const tps::PackKernelFn fn = kernels_for(dst_dtype, wire_dtype).pack[vec];
+    long long grid;
+    if (vec) {
+        grid = (static_cast<long long>(nelem / V) + 255) / 256;
+    } else {
+        grid = (static_cast<long long>(nelem) + 255) / 256;
+        if (grid > c.sm_count * 8ll) grid = c.sm_count * 8ll;
+    }
+    if (grid < 1) grid = 1;
+    fn<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, wire, nelem);
+    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    return AR_OK;
+}
+
 }  // extern "C"

@@ -16,7 +16,12 @@ struct VecKernels {
     KernelFn many[2];  // R >= 3: ranks loaded four at a time
 };
 
+using ExKernelFn = void (*)(ArExParams);
+using PackKernelFn = void (*)(const void *, void *, unsigned long long);
+
 struct Kernels {
+    ExKernelFn ex[2][2][2];  // [R >= 3][residual][16-byte vectors]
+    PackKernelFn pack[2];    // [16-byte vectors]
     VecKernels v16;    // 16-byte vectors
     VecKernels wide;   // the bandwidth width: 32-byte vectors for f32, 16 for 16-bit types
     int wide_bytes;    // 32 or 16
@@ -47,6 +52,16 @@ Kernels make_kernels() {
         k.wide = k.v16;
         k.wide_bytes = 16;
     }
+    k.ex[0][0][0] = ar_reduce_ex_kernel<Td, Tw, 2, false, false>;
+    k.ex[0][0][1] = ar_reduce_ex_kernel<Td, Tw, 2, false, true>;
+    k.ex[0][1][0] = ar_reduce_ex_kernel<Td, Tw, 2, true, false>;
+    k.ex[0][1][1] = ar_reduce_ex_kernel<Td, Tw, 2, true, true>;
+    k.ex[1][0][0] = ar_reduce_ex_kernel<Td, Tw, 4, false, false>;
+    k.ex[1][0][1] = ar_reduce_ex_kernel<Td, Tw, 4, false, true>;
+    k.ex[1][1][0] = ar_reduce_ex_kernel<Td, Tw, 4, true, false>;
+    k.ex[1][1][1] = ar_reduce_ex_kernel<Td, Tw, 4, true, true>;
+    k.pack[0] = ar_pack_kernel<Td, Tw, false>;
+    k.pack[1] = ar_pack_kernel<Td, Tw, true>;
     k.scalar[0] = ar_scalar_kernel<Td, Tw, false>;
     k.scalar[1] = ar_scalar_kernel<Td, Tw, true>;
     k.naive = ar_naive_kernel<Td, Tw>;

@@ -151,3 +151,61 @@ def test_binding_raises_on_error():
     with pytest.raises(tps.ARError) as e:
         tps.ar_query("ranks")
     assert e.value.status == NOT_INIT
+
+
+def lay(**kw):
+    return tps.make_layout(**kw)
+
+
+def chk_l(R=2, srcs=None, dsts=None, max_elems=1 << 20, dst="f32", wire="bf16", **kw):
+    if srcs is None:
+        srcs = [0x1000000 * (k + 1) for k in range(R)]
+    if dsts is None:
+        dsts = [0x40000000]
+    kw.setdefault("ne0", 64)
+    kw.setdefault("ne1", 4)
+    return tps.ar_check_layout(R, srcs, dsts, lay(**kw), max_elems, dst, wire)
+
+
+def test_check_layout_basics():
+    assert chk_l() == OK
+    assert chk_l(ne0=0) == OK and chk_l(ne1=0) == OK  # empty: nothing touched
+    assert chk_l(ne0=1024, ne1=1025, max_elems=1 << 20) == TOO_LARGE
+    assert chk_l(dst=5) == UNSUPPORTED
+    assert chk_l(srcs=[0x1000000, 0]) == INVALID
+    assert chk_l(srcs=[0x1000002, 0x2000000]) == INVALID  # misaligned f32
+
+
+def test_check_layout_strides():
+    assert chk_l(src_row_bytes=[256, 512]) == OK
+    assert chk_l(src_row_bytes=[255, 256]) == INVALID    # shorter than a row (64 x 4 bytes)
+    assert chk_l(src_row_bytes=[258, 256]) == INVALID    # not a multiple of the element size
+    assert chk_l(dst_row_bytes=[300]) == OK
+    assert chk_l(dst_row_bytes=[100]) == INVALID
+    assert chk_l(ne1=1, src_row_bytes=[0, 0]) == OK      # one row: the stride is never used
+
+
+def test_check_layout_inactive_ranks():
+    assert chk_l(srcs=[0x1000000, 0], inactive=(1,)) == OK     # NULL allowed for an inactive rank
+    assert chk_l(srcs=[0, 0], inactive=(0, 1)) == OK
+    assert chk_l(inactive=(2,)) == INVALID                    # bit beyond R
+
+
+def test_check_layout_residual_and_overlap():
+    n = 64 * 4 * 4  # bytes of one 64 x 4 f32 tensor
+    assert chk_l(residual=0x3000000, residual_row_bytes=256) == OK
+    assert chk_l(residual=0x3000000, residual_row_bytes=0) == OK      # bias row
+    assert chk_l(residual=0x3000000, residual_row_bytes=200) == INVALID
+    # in place into the residual: same pointer, same stride
+    assert chk_l(residual=0x40000000, residual_row_bytes=256) == OK
+    assert chk_l(residual=0x40000000, residual_row_bytes=512, dst_row_bytes=[256]) == OVERLAP
+    # destination into a broadcast bias row: overlap
+    assert chk_l(residual=0x40000000, residual_row_bytes=0) == OVERLAP
+    # in place into a source, and a partial overlap
+    assert chk_l(dsts=[0x1000000]) == OK
+    assert chk_l(dsts=[0x1000000 + 128]) == OVERLAP
+    assert chk_l(dsts=[0x1000000 + n]) == OK
+    # two destinations overlapping
+    assert chk_l(dsts=[0x40000000, 0x40000000 + 64]) == OVERLAP
+    # an inactive rank's pointer is never read, so it cannot overlap
+    assert chk_l(srcs=[0x1000000, 0x40000000 + 8], inactive=(1,)) == OK

@@ -1,0 +1,230 @@
+"""GPU parity of the extended layouts (ar_reduce_ex: row strides, inactive
+ranks, residual and row-broadcast bias) and of the wire pack, against the
+oracle, bit for bit (any NaN matches any NaN)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_partial_sum_gb300 as tps
+from tests.gpu_util import TORCH_DTYPE, to_device, to_host
+from tests.libcasts import assert_same, lib_round
+from tests.test_oracle_fold import edgy_f32
+
+pytestmark = pytest.mark.gpu
+
+TYPES = ["f32", "f16", "bf16"]
+PAIRS = list(itertools.product(TYPES, TYPES))
+ES = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_partial_sum_gb300 import build
+    build.build()
+    yield
+    tps.ar_free()
+
+
+def srcs_for(seed, R, n, dst):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [lib_round(dst, edgy_f32(rng, n)) for _ in range(R)]
+
+
+def strided_device(flat_rows, ne0, ne1, stride_elems, dst, lead=0, fill=0x5A):
+    """Device buffer holding ne1 rows at stride_elems (elements), starting
+    `lead` elements into a poisoned allocation; returns (view start tensor,
+    backing bytes)."""
+    es = ES[dst]
+    total = lead + (ne1 - 1) * stride_elems + ne0 if ne1 else lead + 1
+    back = torch.full((total * es + 64,), fill, dtype=torch.uint8, device="cuda")
+    t = back[:total * es].view(TORCH_DTYPE[dst])
+    if flat_rows is not None:
+        dev = to_device(flat_rows, dst)
+        for j in range(ne1):
+            t[lead + j * stride_elems: lead + j * stride_elems + ne0].copy_(dev[j * ne0:(j + 1) * ne0])
+    return t[lead:], back
+
+
+def rows_of(t, ne0, ne1, stride_elems, dst):
+    h = to_host(t, dst)
+    return np.concatenate([h[j * stride_elems: j * stride_elems + ne0] for j in range(ne1)]) if ne1 else h[:0]
+
+
+def run_ex(R, ne0, ne1, dst, wire, seed, src_pad=None, dst_pad=(0,), lead=0, inactive=(), residual=None,
+           bias=False, n_dsts=1):
+    """Run ar_reduce_ex and the oracle on the same strided inputs."""
+    es = ES[dst]
+    src_pad = src_pad or [0] * R
+    srcs = srcs_for(seed, R, ne0 * ne1, dst)
+    tps.ar_init(R, max(1, ne0 * ne1))
+    s_t = []
+    for r in range(R):
+        if r in inactive:
+            s_t.append(None)
+            continue
+        t, _ = strided_device(srcs[r], ne0, ne1, ne0 + src_pad[r], dst, lead=lead)
+        s_t.append(t)
+    d_t, d_backs = [], []
+    pads = list(dst_pad) + [0] * (n_dsts - len(dst_pad))
+    for d in range(n_dsts):
+        t, back = strided_device(None, ne0, ne1, ne0 + pads[d], dst, lead=lead)
+        d_t.append(t)
+        d_backs.append(back)
+    res_t = res_np = None
+    res_stride = None
+    if residual:
+        res_np = srcs_for(seed + 1, 1, ne0 if bias else ne0 * ne1, dst)[0]
+        V = 16 // es
+        rpad = V if ne0 % V == 0 else 3  # aligned rows stay aligned; others get an odd stride
+        res_t, _ = strided_device(res_np, ne0, 1 if bias else ne1, ne0 + (0 if bias else rpad), dst, lead=lead)
+        res_stride = 0 if bias else (ne0 + rpad) * es
+    layout = tps.make_layout(ne0, ne1, src_row_bytes=[(ne0 + p) * es for p in src_pad],
+                             dst_row_bytes=[(ne0 + p) * es for p in pads], residual=res_t,
+                             residual_row_bytes=res_stride, inactive=inactive)
+    tps.ar_reduce_ex(s_t, d_t, layout, dst, wire)
+    torch.cuda.synchronize()
+    holes = [None if r in inactive else s for r, s in enumerate(srcs)]
+    exp = oracle.reduce_2d(holes, 1, dst, wire, ne0, ne1, inactive=inactive, residual=res_np,
+                           residual_stride=0 if bias else None)[0]
+    for d, t in enumerate(d_t):
+        assert_same(rows_of(t, ne0, ne1, ne0 + pads[d], dst), exp, dst,
+                    f"ex R={R} {ne0}x{ne1} inactive={inactive} residual={residual} bias={bias} d={d}")
+    return d_backs
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_packed_2d_all_pairs(dst, wire, R):
+    run_ex(R, 4096 + 5, 7, dst, wire, seed=R * 3 + len(dst + wire), n_dsts=2)
+
+
+@pytest.mark.parametrize("dst,wire", [("f32", "bf16"), ("bf16", "bf16"), ("f16", "f32")])
+@pytest.mark.parametrize("ne0,ne1", [(1, 1), (3, 5), (7, 3), (8, 2), (64, 300), (1000, 3), (4097, 2),
+                                     (100_000, 1)])
+def test_shapes(dst, wire, ne0, ne1):
+    run_ex(3, ne0, ne1, dst, wire, seed=ne0 + ne1, n_dsts=2)
+
+
+@pytest.mark.parametrize("dst", TYPES)
+@pytest.mark.parametrize("kind", ["aligned", "odd_strides", "odd_start"])
+def test_row_strides(dst, kind):
+    """Padded rows (ne0 = 777 leaves a ragged tail in every row): strides
+    that are multiples of 16 bytes take the vector path with a per-row tail,
+    odd strides or an odd start the element-wise path; the padding between
+    rows is never written."""
+    ne0, ne1, es = 777, 9, ES[dst]
+    V = 16 // es
+    base = (V - ne0 % V) % V
+    if kind == "odd_strides":
+        pads, lead = [1, 2, 3], 0
+    else:
+        pads, lead = [base + k * V for k in (1, 2, 3)], (1 if kind == "odd_start" else 0)
+    backs = run_ex(3, ne0, ne1, dst, "bf16", seed=11, src_pad=pads, dst_pad=(pads[0], base), lead=lead, n_dsts=2)
+    b = backs[0].cpu().numpy()
+    stride = (ne0 + pads[0]) * es
+    for j in range(ne1 - 1):
+        gap = b[lead * es + j * stride + ne0 * es: lead * es + (j + 1) * stride]
+        assert (gap == 0x5A).all(), "padding written"
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("inactive", [(0,), (1,), (0, 2), (0, 1, 2)])
+def test_inactive_ranks(dst, wire, inactive):
+    run_ex(3, 5000, 3, dst, wire, seed=21, inactive=inactive)
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("bias", [False, True])
+@pytest.mark.parametrize("ne0", [4096, 4099])
+def test_residual_and_bias(dst, wire, bias, ne0):
+    """ne0 = 4096 keeps every row 16-byte aligned (vector path, residual row
+    padded to a 16-byte stride); 4099 runs element by element."""
+    run_ex(2, ne0, 6, dst, wire, seed=31, residual=True, bias=bias, n_dsts=2)
+
+
+@pytest.mark.parametrize("R", [2, 5])
+def test_residual_bias_inactive_strided_together(R):
+    run_ex(R, 1031, 17, "f32", "f16", seed=41, src_pad=[4 * (r + 1) for r in range(R)], dst_pad=(12,),
+           inactive=(1,), residual=True, bias=True)
+
+
+def test_residual_in_place():
+    """x = x + allreduce(partials): the destination is the residual."""
+    R, ne0, ne1 = 2, 8192, 16
+    srcs = srcs_for(51, R + 1, ne0 * ne1, "f32")
+    tps.ar_init(R, ne0 * ne1)
+    s_t = [to_device(s, "f32") for s in srcs[:R]]
+    x = to_device(srcs[R], "f32")
+    tps.ar_reduce_ex(s_t, [x], tps.make_layout(ne0, ne1, residual=x), "f32", "bf16")
+    torch.cuda.synchronize()
+    exp = oracle.reduce_2d(srcs[:R], 1, "f32", "bf16", ne0, ne1, residual=srcs[R])[0]
+    assert_same(to_host(x, "f32"), exp, "f32", "residual in place")
+
+
+def test_ex_packed_equals_ar_reduce():
+    """Without strides, residual or inactive ranks, ar_reduce_ex gives the
+    bits ar_reduce gives."""
+    R, n = 4, 1 << 20
+    srcs = srcs_for(61, R, n, "bf16")
+    tps.ar_init(R, n)
+    s_t = [to_device(s, "bf16") for s in srcs]
+    a = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    tps.ar_reduce(s_t, [a], dst_dtype="bf16", wire_dtype="f16")
+    tps.ar_reduce_ex(s_t, [b], tps.make_layout(1024, 1024), "bf16", "f16")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_ex_errors_write_nothing():
+    tps.ar_init(2, 1 << 16)
+    a = torch.randn(4096, device="cuda")
+    out = torch.full((4096,), 7.0, device="cuda")
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce_ex([a, a], [out], tps.make_layout(64, 64, src_row_bytes=[100, 256]), "f32", "bf16")
+    assert e.value.status == 1
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce_ex([a, None], [out], tps.make_layout(64, 64), "f32", "bf16")  # NULL active rank
+    assert e.value.status == 1
+    with pytest.raises(tps.ARError) as e:
+        tps.ar_reduce_ex([a, a], [a[8:]], tps.make_layout(64, 63), "f32", "bf16")
+    assert e.value.status == 5
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 4099, 1_000_003])
+def test_wire_pack(dst, wire, n):
+    (x,) = srcs_for(n + 71, 1, n, dst)
+    tps.ar_init(1, max(n, 1))
+    src = to_device(x, dst)
+    out = torch.empty(n, dtype=TORCH_DTYPE[wire], device="cuda")
+    tps.ar_wire_pack(src, out, dst_dtype=dst, wire_dtype=wire)
+    torch.cuda.synchronize()
+    assert_same(to_host(out, wire), oracle.wire_pack(x, dst, wire), wire, f"pack {dst}->{wire} n={n}")
+
+
+@pytest.mark.parametrize("dst,wire", [("f32", "bf16"), ("bf16", "f32"), ("f16", "bf16")])
+def test_wire_pack_unaligned_and_in_place(dst, wire):
+    n = 10_001
+    (x,) = srcs_for(81, 1, n, dst)
+    tps.ar_init(1, n)
+    back = torch.zeros(n + 1, dtype=TORCH_DTYPE[dst], device="cuda")
+    src = back[1:]
+    src.copy_(to_device(x, dst))
+    out_back = torch.zeros(n + 1, dtype=TORCH_DTYPE[wire], device="cuda")
+    out = out_back[1:]
+    tps.ar_wire_pack(src, out, dst_dtype=dst, wire_dtype=wire)
+    torch.cuda.synchronize()
+    exp = oracle.wire_pack(x, dst, wire)
+    assert_same(to_host(out, wire), exp, wire, "pack unaligned")
+    if ES[dst] == ES[wire]:
+        tps.ar_wire_pack(src, src, dst_dtype=dst, wire_dtype=wire)
+        torch.cuda.synchronize()
+        assert_same(to_host(src.view(TORCH_DTYPE[wire]), wire), exp, wire, "pack in place")
