@@ -179,24 +179,44 @@ def gpu_id_for(device_index: int) -> str:
 
 # ---- the oracle as CPU baseline ------------------------------------------------
 
-def oracle_rate(srcs, w, seconds: float):
-    """Time the oracle (single thread, as it stands) on a prefix sample of the
-    workload sized to take about ``seconds``; returns (GB/s, sample text)."""
+def oracle_step(w, srcs, rows: int, out=None):
+    """The oracle's version of one step over the first `rows` rows."""
     import oracle
-    probe = min(w.nelem, 1 << 16)
+    n = rows * w.ne0
+    if w.op == "pack":
+        return oracle.wire_pack(srcs[0][:n], w.dst, w.wire)
+    if w.op == "reduce":
+        return oracle.reduce([s[:n] for s in srcs[:w.R]], w.n_dsts, w.dst, w.wire, out=out)
+    res, res_stride = None, None
+    if w.residual == "full":
+        res = srcs[w.R][:n]
+    elif w.residual == "row":
+        res, res_stride = srcs[w.R], 0
+    holes = [None if r in w.inactive else s[:n] for r, s in enumerate(srcs[:w.R])]
+    return oracle.reduce_2d(holes, w.n_dsts, w.dst, w.wire, w.ne0, rows, inactive=w.inactive, residual=res,
+                            residual_stride=res_stride)
+
+
+def oracle_rate(srcs, w, seconds: float, steps: int = 0):
+    """Time the oracle (single thread, as it stands) on a sample of whole rows
+    of the workload.  With steps == 0 the sample and repetitions are sized to
+    take about `seconds`; otherwise `steps` repetitions of a sample sized to
+    take about seconds / steps each.  Returns (GB/s, elapsed, sample text)."""
+    probe_rows = max(1, min(w.ne1, (1 << 16) // w.ne0))
     t = time.perf_counter()
-    oracle.reduce([s[:probe] for s in srcs], w.n_dsts, w.dst, w.wire)
-    per_elem = max((time.perf_counter() - t) / probe, 1e-9)
-    n = int(min(w.nelem, max(probe, seconds / per_elem)))
-    reps = max(1, int(seconds / (per_elem * n)))
-    sample = [s[:n] for s in srcs]
-    out = None
+    oracle_step(w, srcs, probe_rows)
+    per_row = max((time.perf_counter() - t) / probe_rows, 1e-9)
+    budget = seconds / steps if steps else seconds
+    rows = int(min(w.ne1, max(1, budget / per_row)))
+    reps = steps if steps else max(1, int(seconds / (per_row * rows)))
     t = time.perf_counter()
     for _ in range(reps):
-        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
+        oracle_step(w, srcs, rows)
     el = time.perf_counter() - t
-    moved = (w.R + w.n_dsts) * n * w.elem_bytes * reps
-    return moved / el / 1e9, el, f"first {n} of {w.nelem} elements of each rank, {reps} pass(es), {el:.1f} s"
+    moved = w.bytes_per_call * rows / w.ne1 * reps
+    return (moved / el / 1e9, el,
+            f"first {rows} of {w.ne1} rows ({rows * w.ne0} of {w.nelem} elements) of the workload, "
+            f"{reps} pass(es), {el:.1f} s")
 
 
 # ---- our arm -----------------------------------------------------------------
@@ -231,26 +251,62 @@ def run_ours(args):
 
     # rotating buffer sets: each step's inputs were last touched sets-1 steps ago
     nsets = 1 if w.bytes_per_call >= 3 * l2 else math.ceil(3 * l2 / w.bytes_per_call)
-    base_src = [dev_tensor(a) for a in srcs_np]
+    ne0, ne1, pad = w.ne0, w.ne1, w.row_pad
+
+    def rows_tensor(a=None):
+        """A device tensor of ne1 rows at a row stride of ne0 + pad elements."""
+        t = torch.empty((ne1, ne0 + pad), dtype=tdt, device=dev)
+        if pad:
+            t[:, ne0:].fill_(0)
+        if a is not None:
+            t[:, :ne0].copy_(dev_tensor(a).view(ne1, ne0))
+        return t
+
+    base_src = [dev_tensor(a) if pad == 0 else rows_tensor(a) for a in srcs_np[:w.R]]
+    residual_base = dev_tensor(srcs_np[w.R]) if w.residual else None
     sets = []
     for k in range(nsets):
         s = base_src if k == 0 else [b.clone() for b in base_src]
-        d = [torch.empty(w.nelem, dtype=tdt, device=dev) for _ in range(w.n_dsts)]
-        sets.append((s, d))
+        if w.op == "pack":
+            d = [torch.empty(w.nelem, dtype={"f32": torch.float32, "f16": torch.float16,
+                                             "bf16": torch.bfloat16}[w.wire], device=dev)]
+        else:
+            d = [torch.empty(w.nelem, dtype=tdt, device=dev) if pad == 0 else rows_tensor()
+                 for _ in range(w.n_dsts)]
+        res = None if residual_base is None else (residual_base if k == 0 else residual_base.clone())
+        sets.append((s, d, res))
     stream = torch.cuda.Stream(dev)
     tps.ar_init(w.R, w.nelem)
     if args.bw_blocks_per_sm:
         tps.ar_set_option("bw_blocks_per_sm", args.bw_blocks_per_sm)
+    es = w.elem_bytes
+    layouts = []
+    for s, d, res in sets:
+        if w.op != "reduce_ex":
+            layouts.append(None)
+            continue
+        layouts.append(tps.make_layout(
+            ne0, ne1, src_row_bytes=[(ne0 + pad) * es] * w.R, dst_row_bytes=[(ne0 + pad) * es] * w.n_dsts,
+            residual=res, residual_row_bytes=0 if w.residual == "row" else None, inactive=w.inactive))
+        for r in w.inactive:
+            s[r] = None
 
     def step(i):
-        s, d = sets[i % nsets]
-        tps.ar_reduce(s, d, nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire, stream=stream)
+        k = i % nsets
+        s, d, res = sets[k]
+        if w.op == "reduce":
+            tps.ar_reduce(s, d, nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire, stream=stream)
+        elif w.op == "reduce_ex":
+            tps.ar_reduce_ex(s, d, layouts[k], w.dst, w.wire, stream=stream)
+        else:
+            tps.ar_wire_pack(s[0], d[0], nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
     torch.cuda.synchronize(dev)
-    variant = {v: k for k, v in tps.ar.VARIANTS.items()}[tps.ar_query("last_variant")]
+    variant = ({v: k for k, v in tps.ar.VARIANTS.items()}[tps.ar_query("last_variant")]
+               if w.op == "reduce" else w.op)
 
     # graph of G steps, replayed back to back in the timed region
     G = max(1, min(args.steps, nsets * max(1, math.ceil(64 / nsets))))
@@ -323,10 +379,10 @@ def run_ours(args):
 
     # end to end through the host entry point: pinned host partials in,
     # pinned host results out, every step inside the timed region
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and w.op == "reduce":
         h_srcs = [torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory() for a in srcs_np]
         h_dsts = [torch.empty(w.nelem, dtype=h_srcs[0].dtype).pin_memory() for _ in range(w.n_dsts)]
-        d_srcs, d_dsts = sets[0]
+        d_srcs, d_dsts, _ = sets[0]
 
         def e2e_time(staged: bool) -> float:
             def one():
@@ -356,7 +412,7 @@ def run_ours(args):
                          "staged_pipeline_call": "ar_reduce_host with device staging: chunked H2D copy, kernel, "
                                                  "D2H copy on three streams"}
 
-    del sets, base_src
+    del sets, base_src, residual_base
     torch.cuda.empty_cache()
     if args.decode:
         result["decode"] = bench_decode(dev, stream)
@@ -438,32 +494,18 @@ def run_reference(args):
     if rank != 0:
         return
     from tensor_partial_sum_gb300 import workloads as W
-    import oracle
 
     w = W.WORKLOADS[args.workload]
     srcs = W.generate(w)
-    probe = min(w.nelem, 1 << 16)
-    t = time.perf_counter()
-    oracle.reduce([s[:probe] for s in srcs], w.n_dsts, w.dst, w.wire)
-    per_elem = max((time.perf_counter() - t) / probe, 1e-9)
-    budget = args.ref_seconds / max(1, args.steps + args.warmup)
-    n = int(min(w.nelem, max(256, budget / per_elem)))
-    sample = [s[:n] for s in srcs]
-    out = None
-    for _ in range(args.warmup):
-        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        out = oracle.reduce(sample, w.n_dsts, w.dst, w.wire, out=out)
-    el = time.perf_counter() - t
-    value = (w.R + w.n_dsts) * n * w.elem_bytes * args.steps / el / 1e9
-    text = f"first {n} of {w.nelem} elements of each rank per step"
+    budget = args.ref_seconds
+    # untimed warm-up passes on a small sample, then the timed steps
+    oracle_rate(srcs, w, min(1.0, budget / 10), steps=args.warmup)
+    value, el, text = oracle_rate(srcs, w, budget, steps=args.steps)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.describe()}", "bytes_per_step": (w.R + w.n_dsts) * n * w.elem_bytes,
-                   "parallelism": "oracle on rank 0 only"},
+        "config": {"workload": f"{w.name}: {w.describe()}", "parallelism": "oracle on rank 0 only"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": text},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)

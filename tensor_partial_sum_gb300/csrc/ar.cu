@@ -645,8 +645,10 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     }
     const bool vec = bits % 16 == 0;
     const tps::Kernels &k = kernels_for(dst_dtype, wire_dtype);
-    const tps::ExKernelFn fn = k.ex[c.R > 2][L->residual != nullptr][vec];
-    const size_t V = 16 / es;
+    const bool vec32 = bits % 32 == 0 && k.ex32[0][0] != nullptr;
+    const tps::ExKernelFn fn =
+        vec32 ? k.ex32[c.R > 2][L->residual != nullptr] : k.ex[c.R > 2][L->residual != nullptr][vec];
+    const size_t V = (vec32 ? 32 : 16) / es;
     int threads = 256;
     long long gx;
     if (vec) {
@@ -680,10 +682,13 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
     if (dev != c.device) return AR_ERR_INVALID_ARG;
     if (c.fault_inject) return AR_ERR_CUDA;
-    const size_t V = 16 / es;
-    const size_t out_bytes = V * ew;  // wire bytes per 16-byte source vector
-    const bool vec = a % 16 == 0 && b % (out_bytes > 16 ? out_bytes : 16) == 0;
-    const tps::PackKernelFn fn = kernels_for(dst_dtype, wire_dtype).pack[vec];
+    const tps::Kernels &k = kernels_for(dst_dtype, wire_dtype);
+    // 32-byte source vectors when both buffers allow them, else 16, else element-wise
+    const bool vec32 = k.pack32 != nullptr && a % 32 == 0 && b % (32 / es * ew) == 0;
+    const size_t V = (vec32 ? 32 : 16) / es;
+    const size_t out_bytes = V * ew;  // wire bytes per source vector
+    const bool vec = vec32 || (a % 16 == 0 && b % (out_bytes > 16 ? out_bytes : 16) == 0);
+    const tps::PackKernelFn fn = vec32 ? k.pack32 : k.pack[vec];
     long long grid;
     if (vec) {
         grid = (static_cast<long long>(nelem / V) + 255) / 256;

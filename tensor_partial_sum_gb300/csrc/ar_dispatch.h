@@ -21,7 +21,9 @@ using PackKernelFn = void (*)(const void *, void *, unsigned long long);
 
 struct Kernels {
     ExKernelFn ex[2][2][2];  // [R >= 3][residual][16-byte vectors]
+    ExKernelFn ex32[2][2];   // [R >= 3][residual], 32-byte vectors (f32 only, else nullptr)
     PackKernelFn pack[2];    // [16-byte vectors]
+    PackKernelFn pack32;     // 32-byte source vectors (f32 only, else nullptr)
     VecKernels v16;    // 16-byte vectors
     VecKernels wide;   // the bandwidth width: 32-byte vectors for f32, 16 for 16-bit types
     int wide_bytes;    // 32 or 16
@@ -62,6 +64,13 @@ Kernels make_kernels() {
     k.ex[1][1][1] = ar_reduce_ex_kernel<Td, Tw, 4, true, true>;
     k.pack[0] = ar_pack_kernel<Td, Tw, false>;
     k.pack[1] = ar_pack_kernel<Td, Tw, true>;
+    if constexpr (Td == kF32) {
+        k.ex32[0][0] = ar_reduce_ex_kernel<Td, Tw, 2, false, true, 32>;
+        k.ex32[0][1] = ar_reduce_ex_kernel<Td, Tw, 2, true, true, 32>;
+        k.ex32[1][0] = ar_reduce_ex_kernel<Td, Tw, 4, false, true, 32>;
+        k.ex32[1][1] = ar_reduce_ex_kernel<Td, Tw, 4, true, true, 32>;
+        k.pack32 = ar_pack_kernel<Td, Tw, true, 32>;
+    }
     k.scalar[0] = ar_scalar_kernel<Td, Tw, false>;
     k.scalar[1] = ar_scalar_kernel<Td, Tw, true>;
     k.naive = ar_naive_kernel<Td, Tw>;

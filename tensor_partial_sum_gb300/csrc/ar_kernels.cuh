@@ -397,16 +397,17 @@ __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, 
 }
 
 // Reduction over ne1 rows of ne0 elements.  blockIdx.y strides over rows;
-// within a row, thread t of CTA x owns 16-byte vector x*blockDim.x + t,
+// within a row, thread t of CTA x owns VB-byte vector x*blockDim.x + t,
 // loading RB ranks at a time (inactive ranks are not loaded: their operand
 // is +0), then adds the residual (not rounded through the wire type) after
 // the rank fold, casts once and stores to every destination.  The last CTA
 // in x does the row's tail of fewer than one vector, element by element.
 // VEC = false runs every element through that element-wise path (buffers
 // or strides not 16-byte aligned).
-template <int Td, int Tw, int RB, bool RES, bool VEC>
+template <int Td, int Tw, int RB, bool RES, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant__ ArExParams p) {
-    constexpr int V = 16 / Elem<Td>::bytes;
+    constexpr int NW = VB / 4;
+    constexpr int V = VB / Elem<Td>::bytes;
     const size_t vpr = VEC ? p.ne0 / V : 0;  // whole vectors per row
     const size_t tail0 = vpr * V;
     for (size_t row = blockIdx.y; row < p.ne1; row += gridDim.y) {
@@ -415,43 +416,44 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
             if (v < vpr) {
                 float acc[V];
                 for (int r0 = 0; r0 < p.R; r0 += RB) {
-                    uint32_t w[RB][4];
+                    uint32_t w[RB][NW];
 #pragma unroll
                     for (int j = 0; j < RB; ++j) {
                         const int r = r0 + j;
                         if (r < p.R && !((p.inactive >> r) & 1u)) {
                             const char *base = static_cast<const char *>(p.src[r]) +
-                                               static_cast<long long>(row) * p.src_stride[r] + v * 16;
-                            load_words<16, false>(base, w[j]);
+                                               static_cast<long long>(row) * p.src_stride[r] + v * VB;
+                            load_words<VB, false>(base, w[j]);
                         } else {
-                            w[j][0] = w[j][1] = w[j][2] = w[j][3] = 0u;
+#pragma unroll
+                            for (int k = 0; k < NW; ++k) w[j][k] = 0u;
                         }
                     }
 #pragma unroll
                     for (int j = 0; j < RB; ++j) {
                         if (r0 + j < p.R) {
                             float x[V];
-                            word_operands<Td, Tw, 4>(w[j], x);
+                            word_operands<Td, Tw, NW>(w[j], x);
 #pragma unroll
                             for (int k = 0; k < V; ++k) acc[k] = (r0 + j == 0) ? x[k] : __fadd_rn(acc[k], x[k]);
                         }
                     }
                 }
                 if constexpr (RES) {
-                    uint32_t rw[4];
-                    load_words<16, false>(static_cast<const char *>(p.residual) +
-                                              static_cast<long long>(row) * p.res_stride + v * 16,
+                    uint32_t rw[NW];
+                    load_words<VB, false>(static_cast<const char *>(p.residual) +
+                                              static_cast<long long>(row) * p.res_stride + v * VB,
                                           rw);
                     float x[V];
-                    word_operands<Td, Td, 4>(rw, x);  // widened, no wire rounding
+                    word_operands<Td, Td, NW>(rw, x);  // widened, no wire rounding
 #pragma unroll
                     for (int k = 0; k < V; ++k) acc[k] = __fadd_rn(acc[k], x[k]);
                 }
-                uint32_t out[4];
-                word_pack<Td, 4>(acc, out);
+                uint32_t out[NW];
+                word_pack<Td, NW>(acc, out);
                 for (int d = 0; d < p.n_dsts; ++d)
-                    store_words<16>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d] +
-                                        v * 16,
+                    store_words<VB>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d] +
+                                        v * VB,
                                     out);
             }
             if (blockIdx.x == gridDim.x - 1) {
@@ -468,11 +470,12 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
 
 // Wire pack: wire[i] = T_wire(value(src[i])), the buffer a transport would
 // send (phase 1 of ggml_cuda_ar_kernel in ggml-cuda allreduce.cu).  VEC:
-// each thread converts one 16-byte vector of sources; the last CTA does the
-// tail element by element.
-template <int Td, int Tw, bool VEC>
+// each thread converts one VB-byte vector of sources (16 or 32 bytes); the
+// last CTA does the tail element by element.
+template <int Td, int Tw, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem) {
-    constexpr int V = 16 / Elem<Td>::bytes;
+    constexpr int NW = VB / 4;
+    constexpr int V = VB / Elem<Td>::bytes;
     constexpr int WB = V * Elem<Tw>::bytes;  // output bytes per vector: 8, 16 or 32
     auto one = [&](size_t i) {
         float a = load_elem<Td, false>(src, i);
@@ -487,29 +490,26 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
         const size_t nvec = nelem / V;
         const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         if (v < nvec) {
-            uint32_t w[4];
-            load_words<16, false>(static_cast<const char *>(src) + v * 16, w);  // may run in place
+            uint32_t w[NW];
+            load_words<VB, false>(static_cast<const char *>(src) + v * VB, w);  // may run in place
             float x[V];
-            word_operands<Td, Td, 4>(w, x);  // exact values
+            word_operands<Td, Td, NW>(w, x);  // exact values
             char *o = static_cast<char *>(wire) + v * WB;
+            constexpr int OW = WB / 4;  // output words: 2, 4 or 8
+            uint32_t ow[OW];
             if constexpr (Tw == kF32) {
-                uint32_t ow[V];
 #pragma unroll
                 for (int k = 0; k < V; ++k) ow[k] = __float_as_uint(x[k]);
-                if constexpr (V == 4) {
-                    store_words<16>(o, reinterpret_cast<uint32_t(&)[4]>(ow));
-                } else {
-                    store_words<32>(o, reinterpret_cast<uint32_t(&)[8]>(ow));
-                }
             } else {
-                uint32_t ow[V / 2];
 #pragma unroll
                 for (int k = 0; k < V / 2; ++k) ow[k] = narrow2<Tw>(x[2 * k], x[2 * k + 1]);
-                if constexpr (V == 4) {
-                    asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(o), "r"(ow[0]), "r"(ow[1]) : "memory");
-                } else {
-                    store_words<16>(o, reinterpret_cast<uint32_t(&)[4]>(ow));
-                }
+            }
+            if constexpr (OW == 2) {
+                asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(o), "r"(ow[0]), "r"(ow[1]) : "memory");
+            } else if constexpr (OW == 4) {
+                store_words<16>(o, reinterpret_cast<uint32_t(&)[4]>(ow));
+            } else {
+                store_words<32>(o, reinterpret_cast<uint32_t(&)[8]>(ow));
             }
         }
         if (blockIdx.x == gridDim.x - 1) {

@@ -47,6 +47,19 @@ class Workload:
     seed: int
     values: str
     calls: int = 1
+    # extended layouts (ar_reduce_ex) and the wire pack
+    op: str = "reduce"            # "reduce", "reduce_ex" or "pack"
+    residual: str = ""            # "", "full" (a residual tensor) or "row" (one bias row)
+    row_pad: int = 0              # extra elements between rows (row stride = shape[-1] + row_pad)
+    inactive: tuple = ()          # ranks that contribute +0
+
+    @property
+    def ne0(self) -> int:
+        return self.shape[-1]
+
+    @property
+    def ne1(self) -> int:
+        return self.nelem // self.shape[-1]
 
     @property
     def nelem(self) -> int:
@@ -61,15 +74,32 @@ class Workload:
 
     @property
     def bytes_per_call(self) -> int:
-        """Algorithmic bytes: every source read once, every destination
-        written once."""
-        return (self.R + self.n_dsts) * self.nelem * self.elem_bytes
+        """Algorithmic bytes: every active source (and the residual) read
+        once, every destination written once; row padding is not touched."""
+        es = self.elem_bytes
+        if self.op == "pack":
+            return self.nelem * es + self.nelem * (4 if self.wire == "f32" else 2)
+        n = (self.R - len(self.inactive) + self.n_dsts) * self.nelem * es
+        if self.residual == "full":
+            n += self.nelem * es
+        elif self.residual == "row":
+            n += self.ne0 * es
+        return n
 
     def describe(self) -> str:
         shape = "x".join(str(s) for s in self.shape)
         calls = f" x{self.calls} calls" if self.calls > 1 else ""
+        if self.op == "pack":
+            return f"wire pack {self.dst}[{shape}] -> {self.wire} values={self.values}"
+        extra = ""
+        if self.residual:
+            extra += f" residual={self.residual}"
+        if self.row_pad:
+            extra += f" row_stride={self.ne0 + self.row_pad}"
+        if self.inactive:
+            extra += f" inactive={list(self.inactive)}"
         return (f"R={self.R} {self.dst}[{shape}]{calls} wire={self.wire} n_dsts={self.n_dsts} "
-                f"values={self.values}")
+                f"values={self.values}{extra}")
 
 
 WORKLOADS = {
@@ -79,6 +109,16 @@ WORKLOADS = {
         Workload("prefill", 2, 2, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50"),
         Workload("bf16_t3", 4, 4, "bf16", "bf16", (4096, 8192), 4, "bf16(0.2*t3)"),
         Workload("f16_edges", 8, 1, "f32", "f16", (8192, 8192), 5, "f16-edge mixture"),
+        # the prefill shape through the extended entry points
+        Workload("prefill_residual", 2, 2, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50",
+                 op="reduce_ex", residual="full"),
+        Workload("prefill_bias", 2, 2, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50",
+                 op="reduce_ex", residual="row"),
+        Workload("prefill_strided", 2, 2, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50",
+                 op="reduce_ex", row_pad=64),
+        Workload("prefill_inactive", 2, 2, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50",
+                 op="reduce_ex", inactive=(1,)),
+        Workload("prefill_pack", 1, 1, "f32", "bf16", (2048, 4096), 3, "normal(0,1)+0.1%x50", op="pack"),
     ]
 }
 
@@ -143,7 +183,9 @@ def _rank(w: Workload, rng, n: int, r: int) -> np.ndarray:
 def generate(w: Workload | str, call: int = 0, nelem: int | None = None) -> list:
     """The R source arrays of one call (``call`` selects the per-call seed of
     multi-call workloads).  ``nelem`` draws a shorter prefix-shaped sample
-    with the same recipe (used for small test cases)."""
+    with the same recipe (used for small test cases).  Workloads with a
+    residual get it as one more array after the R sources (a full tensor,
+    or one row for a bias)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
     n = w.nelem if nelem is None else nelem
@@ -154,6 +196,11 @@ def generate(w: Workload | str, call: int = 0, nelem: int | None = None) -> list
         return _rank(w, np.random.Generator(np.random.PCG64(streams[r])), n, r)
 
     if n * w.R < (1 << 22):
-        return [one(r) for r in range(w.R)]
-    with ThreadPoolExecutor(max_workers=min(w.R, os.cpu_count() or 1)) as ex:
-        return list(ex.map(one, range(w.R)))
+        out = [one(r) for r in range(w.R)]
+    else:
+        with ThreadPoolExecutor(max_workers=min(w.R, os.cpu_count() or 1)) as ex:
+            out = list(ex.map(one, range(w.R)))
+    if w.residual:
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(w.R + 1)[w.R]))
+        out.append(_rank(w, rng, w.ne0 if w.residual == "row" else n, w.R))
+    return out

@@ -56,7 +56,7 @@ def rows_of(t, ne0, ne1, stride_elems, dst):
 
 
 def run_ex(R, ne0, ne1, dst, wire, seed, src_pad=None, dst_pad=(0,), lead=0, inactive=(), residual=None,
-           bias=False, n_dsts=1):
+           bias=False, n_dsts=1, res_pad=None):
     """Run ar_reduce_ex and the oracle on the same strided inputs."""
     es = ES[dst]
     src_pad = src_pad or [0] * R
@@ -80,7 +80,7 @@ def run_ex(R, ne0, ne1, dst, wire, seed, src_pad=None, dst_pad=(0,), lead=0, ina
     if residual:
         res_np = srcs_for(seed + 1, 1, ne0 if bias else ne0 * ne1, dst)[0]
         V = 16 // es
-        rpad = V if ne0 % V == 0 else 3  # aligned rows stay aligned; others get an odd stride
+        rpad = res_pad if res_pad is not None else (V if ne0 % V == 0 else 3)  # aligned rows stay aligned
         res_t, _ = strided_device(res_np, ne0, 1 if bias else ne1, ne0 + (0 if bias else rpad), dst, lead=lead)
         res_stride = 0 if bias else (ne0 + rpad) * es
     layout = tps.make_layout(ne0, ne1, src_row_bytes=[(ne0 + p) * es for p in src_pad],
@@ -130,6 +130,17 @@ def test_row_strides(dst, kind):
     for j in range(ne1 - 1):
         gap = b[lead * es + j * stride + ne0 * es: lead * es + (j + 1) * stride]
         assert (gap == 0x5A).all(), "padding written"
+
+
+@pytest.mark.parametrize("wire", TYPES)
+@pytest.mark.parametrize("R", [2, 3])
+def test_f32_32_byte_rows(wire, R):
+    """f32 rows whose starts and strides are all multiples of 32 bytes take
+    the 32-byte vector path (ne0 = 777 leaves a 1-element tail per row)."""
+    ne0 = 777
+    base = (8 - ne0 % 8) % 8
+    run_ex(R, ne0, 11, "f32", wire, seed=91 + R, src_pad=[base + 8 * r for r in range(R)],
+           dst_pad=(base, base + 8), inactive=(1,) if R == 3 else (), residual=True, n_dsts=2, res_pad=base + 16)
 
 
 @pytest.mark.parametrize("dst,wire", PAIRS)

@@ -83,3 +83,55 @@ def test_decode_every_call_graph_captured():
     exp = oracle.reduce(flat, 1, "f32", w.wire)[0].reshape(w.calls, w.nelem)
     for d in range(w.n_dsts):
         assert_same(out[:, d, :].ravel(), exp.ravel(), "f32", f"decode destination {d}")
+
+
+@pytest.mark.parametrize("name", ["prefill_residual", "prefill_bias", "prefill_strided", "prefill_inactive",
+                                  "prefill_pack"])
+def test_full_size_extended_workload(name):
+    """The extended entry points at the prefill size, set up as the benchmark
+    sets them up; the oracle checks a sample of whole rows (the first and last
+    16 and 64 random ones)."""
+    w = W.WORKLOADS[name]
+    srcs = W.generate(w)
+    ne0, ne1, pad, es = w.ne0, w.ne1, w.row_pad, w.elem_bytes
+    tdt = TORCH_DTYPE[w.dst]
+    tps.ar_init(w.R, w.nelem)
+
+    def rows_tensor(a=None):
+        t = torch.zeros((ne1, ne0 + pad), dtype=tdt, device="cuda")
+        if a is not None:
+            t[:, :ne0].copy_(to_device(a, w.dst).view(ne1, ne0))
+        return t
+
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    rows = np.unique(np.concatenate([np.arange(16), np.arange(ne1 - 16, ne1), rng.integers(0, ne1, 64)]))
+    idx = (rows[:, None] * ne0 + np.arange(ne0)[None, :]).ravel()
+    if w.op == "pack":
+        src = to_device(srcs[0], w.dst)
+        out = torch.empty(w.nelem, dtype=TORCH_DTYPE[w.wire], device="cuda")
+        tps.ar_wire_pack(src, out, dst_dtype=w.dst, wire_dtype=w.wire)
+        torch.cuda.synchronize()
+        exp = oracle.wire_pack(srcs[0][idx], w.dst, w.wire)
+        assert_same(to_host(out, w.wire)[idx], exp, w.wire, name)
+        return
+    s_t = [None if r in w.inactive else rows_tensor(srcs[r]) for r in range(w.R)]
+    d_t = [rows_tensor() for _ in range(w.n_dsts)]
+    res_t = to_device(srcs[w.R], w.dst) if w.residual else None
+    layout = tps.make_layout(ne0, ne1, src_row_bytes=[(ne0 + pad) * es] * w.R,
+                             dst_row_bytes=[(ne0 + pad) * es] * w.n_dsts, residual=res_t,
+                             residual_row_bytes=0 if w.residual == "row" else None, inactive=w.inactive)
+    tps.ar_reduce_ex(s_t, d_t, layout, w.dst, w.wire)
+    torch.cuda.synchronize()
+    res, res_stride = None, None
+    if w.residual == "full":
+        res = srcs[w.R][idx]
+    elif w.residual == "row":
+        res, res_stride = srcs[w.R], 0
+    holes = [None if r in w.inactive else srcs[r][idx] for r in range(w.R)]
+    exp = oracle.reduce_2d(holes, 1, w.dst, w.wire, ne0, rows.size, inactive=w.inactive, residual=res,
+                           residual_stride=res_stride)[0]
+    for d in d_t:
+        got = to_host(d[:, :ne0].contiguous(), w.dst).reshape(ne1, ne0)[rows].ravel()
+        assert_same(got, exp, w.dst, name)
+        if pad:
+            assert (d[:, ne0:] == 0).all(), "row padding written"
