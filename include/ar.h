@@ -270,6 +270,44 @@ int ar_check_layout(int R, const void *const *srcs, void *const *dsts, int n_dst
 int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype,
                  cudaStream_t stream);
 
+/*
+ * ar_reduce_host_noalloc -- ar_reduce_host for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this entry point exists
+ * for callers of this library, not because of the method.)
+ *
+ * Who needs it: code that may not call cudaMalloc -- for example a plug-in
+ * running inside a framework whose caching allocator owns the whole device
+ * memory budget, or a latency-critical path that cannot afford cudaMalloc /
+ * cudaFree and the device-wide synchronisation they can cause.  Such
+ * callers cannot provide the device staging buffers ar_reduce_host wants.
+ *
+ * What it does: copies each host source into a fixed staging area built into
+ * the library, reduces there, and copies every destination back to its host
+ * buffer, all enqueued on `stream` (results are valid once `stream` reaches
+ * the end of this call).  It allocates nothing: no cudaMalloc, no cudaFree,
+ * no allocating library routine.  Same arguments and results as
+ * ar_reduce_host with NULL staging arrays, except that the host buffers may
+ * be ordinary pageable memory.
+ *
+ * Limits and rules:
+ *   - The staging area is AR_NOALLOC_SCRATCH_BYTES (64 MiB) of device
+ *     memory that every GPU which loads the library holds until the process
+ *     exits.  A call needs R + n_dsts buffers of nelem elements, each rounded
+ *     up to 256 bytes; a call that needs more returns AR_ERR_TOO_LARGE and
+ *     does nothing.
+ *   - The first call on a device looks up the staging area's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a GPU uses the same staging area, and each call leaves
+ *     its data there: nothing in it has to start at zero, because every call
+ *     writes its inputs before reading them.  Calls whose work overlaps on
+ *     the GPU (two streams, or two threads) race on the staging area and may
+ *     produce wrong results: serialise them, e.g. on one stream.
+ */
+#define AR_NOALLOC_SCRATCH_BYTES (64u << 20)
+int ar_reduce_host_noalloc(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem,
+                           int dst_dtype, int wire_dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.ar_check_layout.restype = i
         L.ar_wire_pack.argtypes = [vp, vp, sz, i, i, vp]
         L.ar_wire_pack.restype = i
+        L.ar_reduce_host_noalloc.argtypes = [pp, pp, i, sz, i, i, vp]
+        L.ar_reduce_host_noalloc.restype = i
         _lib = L
     return _lib
 
@@ -247,3 +249,16 @@ def ar_wire_pack(src, wire, nelem=None, dst_dtype=None, wire_dtype="bf16", strea
         dst_dtype = src.dtype
     _check(lib().ar_wire_pack(_ptr(src), _ptr(wire), nelem, _dtype_code(dst_dtype), _dtype_code(wire_dtype),
                               _stream(stream)), "ar_wire_pack")
+
+
+AR_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def ar_reduce_host_noalloc(h_srcs, h_dsts, nelem=None, dst_dtype=None, wire_dtype="bf16", stream=None) -> None:
+    """Host partials in, host results out, staged through the library's own
+    fixed device area: for callers that may not allocate device memory.
+    At most AR_NOALLOC_SCRATCH_BYTES of staging per call; calls that overlap
+    on the GPU share that area and must not run at the same time."""
+    nelem, dcode = _infer(h_srcs, nelem, dst_dtype)
+    _check(lib().ar_reduce_host_noalloc(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode,
+                                        _dtype_code(wire_dtype), _stream(stream)), "ar_reduce_host_noalloc")

@@ -702,4 +702,75 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     return AR_OK;
 }
 
+// ---- staging without allocation ---------------------------------------------
+//
+// ar_reduce_host_noalloc stages host partials through this fixed array
+// instead of device buffers the caller would have to allocate.  It is part of
+// the library image, so every GPU that loads the library holds it (64 MiB)
+// until the process exits; it is shared by every call on that GPU.
+
+namespace {
+
+static_assert(AR_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[AR_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch per device ordinal, looked up once per
+// device (guarded by g_mu).  In host code the array's name is only a host-side
+// handle, never an address a kernel may use.
+constexpr int kMaxScratchDevices = 64;
+void *g_noalloc_addr[kMaxScratchDevices] = {};
+
+}  // namespace
+
+int ar_reduce_host_noalloc(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem, int dst_dtype,
+                           int wire_dtype, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+    const Context &c = g_ctx;
+    if (!h_srcs || !h_dsts || n_dsts < 1 || n_dsts > AR_MAX_DSTS) return AR_ERR_INVALID_ARG;
+    const size_t es = elem_bytes(dst_dtype);
+    if (!es || !elem_bytes(wire_dtype)) return AR_ERR_UNSUPPORTED;
+    if (nelem > c.max_elems) return AR_ERR_TOO_LARGE;
+    if (nelem == 0) return AR_OK;
+    for (int r = 0; r < c.R; ++r)
+        if (!h_srcs[r]) return AR_ERR_INVALID_ARG;
+    for (int d = 0; d < n_dsts; ++d)
+        if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
+    // every staged buffer starts on a 256-byte boundary of the array
+    const size_t bytes = nelem * es;
+    const size_t slot = (bytes + 255) / 256 * 256;
+    if (slot < bytes || static_cast<size_t>(c.R + n_dsts) > AR_NOALLOC_SCRATCH_BYTES / slot)
+        return AR_ERR_TOO_LARGE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+    if (dev != c.device || dev < 0 || dev >= kMaxScratchDevices) return AR_ERR_INVALID_ARG;
+    if (!g_noalloc_addr[dev]) {
+        // first call on this device (which is current here): find the array's device address
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return AR_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = ptr;
+    }
+    if (c.fault_inject) return AR_ERR_CUDA;
+    char *base = static_cast<char *>(g_noalloc_addr[dev]);
+    const void *d_srcs[AR_MAX_RANKS];
+    void *d_dsts[AR_MAX_DSTS];
+    for (int r = 0; r < c.R; ++r) {
+        d_srcs[r] = base + static_cast<size_t>(r) * slot;
+        if (cudaMemcpyAsync(const_cast<void *>(d_srcs[r]), h_srcs[r], bytes, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess)
+            return AR_ERR_CUDA;
+    }
+    for (int d = 0; d < n_dsts; ++d) d_dsts[d] = base + static_cast<size_t>(c.R + d) * slot;
+    const int st = launch_locked(d_srcs, d_dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, stream,
+                                 false);
+    if (st != AR_OK) return st;
+    for (int d = 0; d < n_dsts; ++d)
+        if (cudaMemcpyAsync(h_dsts[d], d_dsts[d], bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            return AR_ERR_CUDA;
+    return AR_OK;
+}
+
 }  // extern "C"
