@@ -349,3 +349,49 @@ def test_host_entry_direct_rejects_pageable_memory(ctx):
         tps.ar_reduce_host([a, b], [out], nelem=1024, dst_dtype="f32", wire_dtype="bf16")
     assert e.value.status == 1
     assert (out == 7.0).all()
+
+
+@pytest.mark.parametrize("wire", ["bf16", "f16"])
+def test_kernel_casts_on_structured_patterns(ctx, wire):
+    """R = 1 through the kernels is the wire round-trip: every sign,
+    exponent and kept-fraction pattern crossed with the tie-deciding low bits
+    (the inputs the CPU pins check the oracle on), through the bandwidth and
+    latency paths, against the oracle."""
+    from tests.test_oracle_casts import _structured_inputs
+    x = _structured_inputs(wire)
+    exp = oracle.reduce([x], 1, "f32", wire)[0]
+    for v in ("bandwidth", "latency"):
+        outs, _ = run(ctx, [x], 1, "f32", wire, variant=v)
+        assert_same(outs[0], exp, "f32", f"casts {wire} via {v}")
+
+
+def test_concurrent_calls_from_two_threads(ctx):
+    """Two host threads enqueue reductions on their own streams at once; the
+    context is shared and every result is right."""
+    import threading
+    R, n = 3, 200_003
+    ctx.ensure(R, n)
+    cases = []
+    for k in range(2):
+        srcs = srcs_for(300 + k, R, n, "f32")
+        cases.append((srcs, expect(srcs, "f32", "f16"), [to_device(s, "f32") for s in srcs],
+                      torch.empty(n, device="cuda"), torch.cuda.Stream()))
+    errors = []
+
+    def worker(k):
+        try:
+            _, _, s_t, out, stream = cases[k]
+            for _ in range(50):
+                tps.ar_reduce(s_t, [out], dst_dtype="f32", wire_dtype="f16", stream=stream)
+            stream.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for srcs, exp, _, out, _ in cases:
+        assert_same(to_host(out, "f32"), exp, "f32", "concurrent")
