@@ -395,3 +395,31 @@ def test_concurrent_calls_from_two_threads(ctx):
     assert not errors, errors
     for srcs, exp, _, out, _ in cases:
         assert_same(to_host(out, "f32"), exp, "f32", "concurrent")
+
+
+@pytest.mark.exhaustive
+@pytest.mark.parametrize("wire", ["bf16", "f16"])
+def test_kernel_casts_exhaustive(ctx, wire):
+    """Every float32 bit pattern through the kernel with R = 1 (the wire
+    round-trip) against the oracle, in chunks of 2^26; the oracle runs in
+    parallel threads on the host (opt-in: TPS_EXHAUSTIVE=1)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    chunk = 1 << 26
+    ctx.ensure(1, chunk)
+    d_in = torch.empty(chunk, dtype=torch.float32, device="cuda")
+    d_out = torch.empty_like(d_in)
+    h_out = torch.empty(chunk, dtype=torch.float32).pin_memory()
+    nthreads = os.cpu_count() or 8
+    part = chunk // nthreads
+    with ThreadPoolExecutor(nthreads) as pool:
+        for start in range(0, 1 << 32, chunk):
+            x = np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+            d_in.copy_(torch.from_numpy(x))
+            tps.ar_reduce([d_in], [d_out], dst_dtype="f32", wire_dtype=wire)
+            h_out.copy_(d_out)
+            exp = np.empty(chunk, dtype=np.float32)
+            list(pool.map(lambda k: oracle.reduce([x], 1, "f32", wire, begin=k * part,
+                                                  end=chunk if k == nthreads - 1 else (k + 1) * part,
+                                                  out=[exp]), range(nthreads)))
+            assert_same(h_out.numpy(), exp, "f32", f"{wire} chunk {start:#x}")
