@@ -204,8 +204,12 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kLatencyThreads;
             plan_vec_bytes = 16;
-            const long long nv = static_cast<long long>(nelem / (16 / esize));
-            grid = grid_cap((nv + threads - 1) / threads, 0x7FFFFFFFll);
+            const long long V = static_cast<long long>(16 / esize);
+            const long long nv = static_cast<long long>(nelem) / V;
+            // with a tail, at most threads - V vectors per CTA, so the last CTA
+            // has idle threads for the tail
+            const long long per_cta = (static_cast<long long>(nelem) % V) ? threads - V : threads;
+            grid = grid_cap((nv + per_cta - 1) / per_cta, 0x7FFFFFFFll);
             break;
         }
         case AR_VARIANT_BANDWIDTH: {
@@ -217,8 +221,10 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kBandwidthThreads;
             plan_vec_bytes = vec_bytes;
-            const long long nv = static_cast<long long>(nelem / (vec_bytes / esize));
-            const long long full = (nv + threads - 1) / threads;
+            const long long V = static_cast<long long>(vec_bytes / esize);
+            const long long nv = static_cast<long long>(nelem) / V;
+            const long long per_cta = (static_cast<long long>(nelem) % V) ? threads - V : threads;
+            const long long full = (nv + per_cta - 1) / per_cta;
             if (grid_blocks > 0) {
                 grid = grid_blocks;
             } else if (c.bw_blocks_per_sm > 0) {

@@ -159,10 +159,27 @@ __device__ __forceinline__ void store_elem(void *base, size_t i, float v) {
     }
 }
 
+// Round one widened value through the wire type.
+template <int Td, int Tw>
+__device__ __forceinline__ float wire1(float a) {
+    float b = a;
+    wire2<Td, Tw>(a, b);
+    return a;
+}
+
+// One element of every rank: all R loads are issued (predicated on r < R)
+// before the first is used, so the element path waits for memory once, not
+// once per rank; then the operands are folded in ascending rank order.
 template <int Td, int Tw, bool NC>
 __device__ __forceinline__ void reduce_elem(const ArParams &p, size_t i) {
-    float acc = elem_operand<Td, Tw, NC>(p.src[0], i);
-    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, elem_operand<Td, Tw, NC>(p.src[r], i));
+    float v[kMaxRanks];
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; ++r)
+        if (r < p.R) v[r] = load_elem<Td, NC>(p.src[r], i);
+    float acc = wire1<Td, Tw>(v[0]);
+#pragma unroll
+    for (int r = 1; r < kMaxRanks; ++r)
+        if (r < p.R) acc = __fadd_rn(acc, wire1<Td, Tw>(v[r]));
     for (int d = 0; d < p.n_dsts; ++d) store_elem<Td>(p.dst[d], i, acc);
 }
 
@@ -306,7 +323,7 @@ __device__ __forceinline__ void reduce_span(const ArParams &p, size_t first, siz
 // issued before the first conversion (RB*U*VB bytes in flight per thread),
 // then the batch's operands are added in ascending rank order.  Each warp
 // access covers 32 adjacent vectors.  The last CTA also does the tail of
-// fewer than one vector's elements.
+// fewer than one vector's elements, on its highest threads.
 template <int Td, int Tw, int VB, int U, int RB, bool NC>
 __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ ArParams p) {
     constexpr int V = VB / Elem<Td>::bytes;
@@ -325,7 +342,10 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
         }
     }
     if (blockIdx.x == gridDim.x - 1) {
-        const size_t i = nvec * V + threadIdx.x;
+        // the tail goes to the block's highest threads: when the host leaves
+        // them without a vector (it does whenever there is a tail), the tail's
+        // loads overlap the vectors' instead of following them
+        const size_t i = nvec * V + (blockDim.x - 1 - threadIdx.x);
         if (i < p.nelem) reduce_elem<Td, Tw, NC>(p, i);
     }
 }
@@ -375,23 +395,32 @@ struct ArExParams {
     int n_dsts;
 };
 
-// Operand r of element i of row `row`, rounded through the wire type; +0
-// for an inactive rank (the reduction of a zeroed partial).
-template <int Td, int Tw>
-__device__ __forceinline__ float ex_operand(const ArExParams &p, int r, size_t row, size_t i) {
-    if ((p.inactive >> r) & 1u) return 0.0f;
-    const char *base = static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
-    return elem_operand<Td, Tw, false>(base, i);
-}
-
 template <int Td, int Tw, bool RES>
 __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, size_t i) {
-    float acc = ex_operand<Td, Tw>(p, 0, row, i);
-    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, ex_operand<Td, Tw>(p, r, row, i));
+    // all loads first (inactive ranks are +0 and not loaded), then the fold
+    float v[kMaxRanks];
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; ++r) {
+        if (r < p.R) {
+            if ((p.inactive >> r) & 1u) {
+                v[r] = 0.0f;
+            } else {
+                const char *base =
+                    static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
+                v[r] = load_elem<Td, false>(base, i);
+            }
+        }
+    }
+    float res = 0.0f;
     if constexpr (RES) {
         const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
-        acc = __fadd_rn(acc, load_elem<Td, false>(rb, i));
+        res = load_elem<Td, false>(rb, i);
     }
+    float acc = wire1<Td, Tw>(v[0]);
+#pragma unroll
+    for (int r = 1; r < kMaxRanks; ++r)
+        if (r < p.R) acc = __fadd_rn(acc, wire1<Td, Tw>(v[r]));
+    if constexpr (RES) acc = __fadd_rn(acc, res);
     for (int d = 0; d < p.n_dsts; ++d)
         store_elem<Td>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d], i, acc);
 }
