@@ -423,3 +423,42 @@ def test_kernel_casts_exhaustive(ctx, wire):
                                                   end=chunk if k == nthreads - 1 else (k + 1) * part,
                                                   out=[exp]), range(nthreads)))
             assert_same(h_out.numpy(), exp, "f32", f"{wire} chunk {start:#x}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "bandwidth", "latency", "scalar"])
+def test_sixteen_ranks_sixteen_destinations(ctx, variant):
+    """The largest call the ABI allows: R = 16 and n_dsts = 16."""
+    n = 65_539
+    srcs = srcs_for(16161, 16, n, "bf16")
+    exp = expect(srcs, "bf16", "f16")
+    outs, backs = run(ctx, srcs, 16, "bf16", "f16", variant=variant, pad=32)
+    for d, o in enumerate(outs):
+        assert_same(o, exp, "bf16", f"R=16 n_dsts=16 {variant} dst={d}")
+    check_guards(backs)
+
+
+def test_more_than_2_31_elements(ctx):
+    """64-bit indexing: 2^31 + 7 bf16 elements per buffer (4 GiB each), two
+    sources and one destination; the oracle checks the first and last 64 Ki
+    elements and 1 Mi random ones."""
+    n = (1 << 31) + 7
+    ctx.ensure(2, n)
+    rng = np.random.Generator(np.random.PCG64(2031))
+    # cheap deterministic finite bf16 patterns: exponent fields 100..140, any sign and fraction
+    base = np.arange(n, dtype=np.uint32)
+    a = ((base * np.uint32(2654435761)) >> np.uint32(16)).astype(np.uint16)
+    b = ((base * np.uint32(40503)) >> np.uint32(8)).astype(np.uint16)
+    del base
+    for x in (a, b):
+        e = (np.uint16(100) + (x >> np.uint16(7)) % np.uint16(41)).astype(np.uint16)
+        x[:] = (x & np.uint16(0x807F)) | (e << np.uint16(7))
+    d_a, d_b = to_device(a, "bf16"), to_device(b, "bf16")
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    tps.ar_reduce([d_a, d_b], [out], nelem=n, dst_dtype="bf16", wire_dtype="f16")
+    torch.cuda.synchronize()
+    del d_a, d_b
+    k = 1 << 16
+    idx = np.unique(np.concatenate([np.arange(k), np.arange(n - k, n), rng.integers(0, n, 1 << 20)]))
+    got = out.view(torch.int16)[torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
+    exp = oracle.reduce([a[idx], b[idx]], 1, "bf16", "f16")[0]
+    assert_same(got, exp, "bf16", "2^31 + 7 elements")
