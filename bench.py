@@ -288,6 +288,8 @@ def run_ours(args):
     tps.ar_init(w.R, w.nelem)
     if args.bw_blocks_per_sm:
         tps.ar_set_option("bw_blocks_per_sm", args.bw_blocks_per_sm)
+    if args.variant != "auto":
+        tps.ar_set_option("forced_variant", tps.ar.VARIANTS[args.variant])
     es = w.elem_bytes
     layouts = []
     for s, d, res in sets:
@@ -540,6 +542,7 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=60.0)
     p.add_argument("--no-decode", dest="decode", action="store_false")
+    p.add_argument("--variant", default="auto", help="force a kernel variant of ar_reduce (auto, bandwidth, tma, ...)")
     p.add_argument("--bw-blocks-per-sm", type=int, default=0,
                    help="0: bandwidth grid covers the tensor; n: persistent grid of n CTAs per SM")
     args = p.parse_args(argv)

@@ -89,7 +89,13 @@ typedef enum {
     AR_VARIANT_LATENCY = 2,   /* one 16-byte vector per thread, 128-thread CTAs */
     AR_VARIANT_BANDWIDTH = 3, /* one 32-byte (f32) or 16-byte vector per thread, 256-thread
                                  CTAs; all loads of two or four ranks issued together */
-    AR_VARIANT_SCALAR = 4     /* element-wise path used for unaligned pointers */
+    AR_VARIANT_SCALAR = 4,    /* element-wise path used for unaligned pointers */
+    AR_VARIANT_TMA = 5        /* shared-memory staging: a producer warp bulk-copies (cp.async.bulk)
+                                 R source tiles per stage, eight warps fold them, one thread
+                                 bulk-stores the result tile to every destination; one CTA per SM.
+                                 Never chosen by AUTO.  Its internal waits are bounded: a wait
+                                 that runs out sets bit 0 of AR_Q_DEVICE_STATUS and the call's
+                                 results are then unspecified (the call still ends). */
 } ar_variant;
 
 /*
@@ -97,8 +103,11 @@ typedef enum {
  *   R          number of ranks (partials) every ar_reduce call sums, 1..16.
  *   max_elems  largest nelem any later call may pass (>= 1).
  * Reads the environment once: AR_VARIANT (auto|naive|latency|bandwidth|
- * scalar), AR_LATENCY_MAX_BYTES (size switch, bytes of sources plus
- * destinations), AR_LOG=1 (one line per init to stderr).
+ * scalar|tma), AR_LATENCY_MAX_BYTES (size switch, bytes of sources plus
+ * destinations), AR_TMA_STAGES (2..8, default 3), AR_TMA_TILE (largest
+ * tile in bytes, a multiple of 1024 up to 32768, default 16384),
+ * AR_TMA_CTAS_PER_SM (1..4, default 1), AR_LOG=1 (one line per init to
+ * stderr).
  * Calling it again replaces the context.  Returns AR_OK, AR_ERR_INVALID_ARG,
  * AR_ERR_UNSUPPORTED (the device is not sm_103) or AR_ERR_CUDA (no device).
  */
@@ -164,8 +173,11 @@ typedef enum {
                                    before anything is enqueued (host-side test hook) */
     AR_Q_BW_BLOCKS_PER_SM = 8,  /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
                                    persistent grid of n CTAs per SM (capped by occupancy) */
-    AR_Q_HOST_CHUNK_BYTES = 9   /* ar_reduce_host pipeline chunk, bytes per buffer (default 4 MiB;
+    AR_Q_HOST_CHUNK_BYTES = 9,  /* ar_reduce_host pipeline chunk, bytes per buffer (default 4 MiB;
                                    at most 64 chunks per call) */
+    AR_Q_DEVICE_STATUS = 10     /* device-side status word (bit 0: a bounded wait of the TMA
+                                   variant ran out); reading it synchronises with the device;
+                                   set it to 0 to clear it */
 } ar_key;
 
 /* Read one context value into *value.  AR_ERR_NOT_INITIALIZED before init. */

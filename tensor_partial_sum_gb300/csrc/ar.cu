@@ -54,6 +54,10 @@ struct Context {
     int bw_blocks_per_sm = 0;
     int64_t host_chunk_bytes = kDefaultHostChunkBytes;
     HostPipe pipe;
+    unsigned *dev_status = nullptr;  // device word the TMA variant sets when a wait runs out
+    int tma_stages = 3;              // AR_TMA_STAGES (2..8)
+    int tma_tile = 16384;            // AR_TMA_TILE: largest tile, bytes (1024 .. 32768, 1 KiB multiples)
+    int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
 };
 
 void destroy_pipe(HostPipe &p) {
@@ -126,6 +130,7 @@ int blocks_per_sm(KernelFn fn, int threads) {
 
 int parse_variant(const char *s) {
     if (!s || !*s || !strcmp(s, "auto")) return AR_VARIANT_AUTO;
+    if (!strcmp(s, "tma")) return AR_VARIANT_TMA;
     if (!strcmp(s, "naive")) return AR_VARIANT_NAIVE;
     if (!strcmp(s, "latency")) return AR_VARIANT_LATENCY;
     if (!strcmp(s, "bandwidth")) return AR_VARIANT_BANDWIDTH;
@@ -139,6 +144,7 @@ const char *variant_name(int v) {
         case AR_VARIANT_LATENCY: return "latency";
         case AR_VARIANT_BANDWIDTH: return "bandwidth";
         case AR_VARIANT_SCALAR: return "scalar";
+        case AR_VARIANT_TMA: return "tma";
         default: return "auto";
     }
 }
@@ -147,6 +153,39 @@ int grid_cap(long long want, long long cap) {
     if (want < 1) want = 1;
     if (want > cap) want = cap;
     return static_cast<int>(want);
+}
+
+// TMA variant: 3 stages of R source tiles plus two output tiles in shared
+// memory, the tile as large as fits (1 KiB multiples, at most 16 KiB), one
+// CTA per SM (or grid_blocks), every wait bounded by 100 ms.
+constexpr size_t kTmaSmemBudget = 224 * 1024;  // per SM
+
+int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t esize, int grid_blocks,
+                      cudaStream_t stream) {
+    Context &c = g_ctx;
+    tps::TmaPlan plan{};
+    plan.vec_bytes = (static_cast<unsigned long long>(nelem) * esize) / 16 * 16;
+    const size_t S = static_cast<size_t>(c.tma_stages);
+    const size_t budget = kTmaSmemBudget / static_cast<size_t>(c.tma_ctas_per_sm) - tps::kTmaHeaderBytes - 1024;
+    size_t tile = budget / (S * p.R + 2) / 1024 * 1024;
+    if (tile > static_cast<size_t>(c.tma_tile)) tile = static_cast<size_t>(c.tma_tile);
+    if (tile < 1024) return AR_ERR_UNSUPPORTED;
+    plan.tile_bytes = static_cast<unsigned>(tile);
+    plan.stages = static_cast<unsigned>(S);
+    plan.ntiles = (plan.vec_bytes + tile - 1) / tile;
+    plan.status = c.dev_status;
+    plan.timeout_ns = 100ull * 1000 * 1000;
+    const size_t smem = tps::kTmaHeaderBytes + (S * p.R + 2) * tile;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(k.tma), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return AR_ERR_CUDA;
+    long long grid = grid_blocks > 0 ? grid_blocks : static_cast<long long>(c.sm_count) * c.tma_ctas_per_sm;
+    if (grid > static_cast<long long>(plan.ntiles)) grid = static_cast<long long>(plan.ntiles);
+    if (grid < 1) grid = 1;
+    k.tma<<<static_cast<unsigned>(grid), tps::kTmaThreads, smem, stream>>>(p, plan);
+    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    c.last_variant = AR_VARIANT_TMA;
+    return AR_OK;
 }
 
 // Launch one reduction; the caller holds g_mu and has validated the arguments.
@@ -175,7 +214,7 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         const double bytes = static_cast<double>(c.R + n_dsts) * static_cast<double>(nelem) * esize;
         variant = bytes < static_cast<double>(c.latency_max_bytes) ? AR_VARIANT_LATENCY : AR_VARIANT_BANDWIDTH;
     }
-    if (!aligned && (variant == AR_VARIANT_LATENCY || variant == AR_VARIANT_BANDWIDTH)) {
+    if (!aligned && (variant == AR_VARIANT_LATENCY || variant == AR_VARIANT_BANDWIDTH || variant == AR_VARIANT_TMA)) {
         if (explicit_variant) return AR_ERR_INVALID_ARG;
         variant = AR_VARIANT_SCALAR;
     }
@@ -242,6 +281,8 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             grid = grid_cap(grid_blocks > 0 ? cap : (static_cast<long long>(nelem) + threads - 1) / threads, cap);
             break;
         }
+        case AR_VARIANT_TMA:
+            return launch_tma_locked(k, p, nelem, esize, grid_blocks, stream);
         case AR_VARIANT_NAIVE: {
             fn = k.naive;
             threads = kScalarThreads;
@@ -368,6 +409,7 @@ int ar_init(int R, size_t max_elems) {
 
     std::lock_guard<std::mutex> lock(g_mu);
     destroy_pipe(g_ctx.pipe);
+    if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
     g_ctx = Context{};
     int dev = -1, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
@@ -385,6 +427,19 @@ int ar_init(int R, size_t max_elems) {
     c.device = dev;
     c.sm_count = sms;
     c.forced_variant = variant;
+    auto env_int = [](const char *name, int lo, int hi, int *out) {
+        const char *s = getenv(name);
+        if (!s) return true;
+        char *end = nullptr;
+        const long v = strtol(s, &end, 10);
+        if (end == s || v < lo || v > hi) return false;
+        *out = static_cast<int>(v);
+        return true;
+    };
+    if (!env_int("AR_TMA_STAGES", 2, tps::kTmaMaxStages, &c.tma_stages) ||
+        !env_int("AR_TMA_TILE", 1024, 32768, &c.tma_tile) || c.tma_tile % 1024 ||
+        !env_int("AR_TMA_CTAS_PER_SM", 1, 4, &c.tma_ctas_per_sm))
+        return AR_ERR_INVALID_ARG;
     if (const char *s = getenv("AR_LATENCY_MAX_BYTES")) {
         char *end = nullptr;
         const long long v = strtoll(s, &end, 10);
@@ -392,6 +447,11 @@ int ar_init(int R, size_t max_elems) {
         c.latency_max_bytes = v;
     }
     if (!create_pipe(c.pipe)) return AR_ERR_CUDA;
+    if (cudaMalloc(reinterpret_cast<void **>(&c.dev_status), 64) != cudaSuccess ||
+        cudaMemset(c.dev_status, 0, 64) != cudaSuccess) {
+        destroy_pipe(c.pipe);
+        return AR_ERR_CUDA;
+    }
     c.ready = true;
     g_ctx = c;
     if (const char *s = getenv("AR_LOG"); s && !strcmp(s, "1")) {
@@ -404,12 +464,13 @@ int ar_init(int R, size_t max_elems) {
 void ar_free(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     destroy_pipe(g_ctx.pipe);
+    if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
     g_ctx = Context{};
 }
 
 int ar_reduce_variant(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
                       int wire_dtype, int variant, int grid_blocks, cudaStream_t stream) {
-    if (variant < AR_VARIANT_AUTO || variant > AR_VARIANT_SCALAR || grid_blocks < 0) return AR_ERR_INVALID_ARG;
+    if (variant < AR_VARIANT_AUTO || variant > AR_VARIANT_TMA || grid_blocks < 0) return AR_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
     const int st = ar_check_args(g_ctx.R, srcs, dsts, n_dsts, nelem, g_ctx.max_elems, dst_dtype, wire_dtype);
@@ -439,6 +500,12 @@ int ar_query(int key, int64_t *value) {
         case AR_Q_FAULT_INJECT: *value = c.fault_inject; break;
         case AR_Q_BW_BLOCKS_PER_SM: *value = c.bw_blocks_per_sm; break;
         case AR_Q_HOST_CHUNK_BYTES: *value = c.host_chunk_bytes; break;
+        case AR_Q_DEVICE_STATUS: {
+            unsigned v = 0;
+            if (cudaMemcpy(&v, c.dev_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return AR_ERR_CUDA;
+            *value = v;
+            break;
+        }
         default: return AR_ERR_INVALID_ARG;
     }
     return AR_OK;
@@ -454,7 +521,7 @@ int ar_set_option(int key, int64_t value) {
             c.latency_max_bytes = value;
             break;
         case AR_Q_FORCED_VARIANT:
-            if (value < AR_VARIANT_AUTO || value > AR_VARIANT_SCALAR) return AR_ERR_INVALID_ARG;
+            if (value < AR_VARIANT_AUTO || value > AR_VARIANT_TMA) return AR_ERR_INVALID_ARG;
             c.forced_variant = static_cast<int>(value);
             break;
         case AR_Q_FAULT_INJECT: c.fault_inject = value ? 1 : 0; break;
@@ -465,6 +532,10 @@ int ar_set_option(int key, int64_t value) {
         case AR_Q_HOST_CHUNK_BYTES:
             if (value < 1) return AR_ERR_INVALID_ARG;
             c.host_chunk_bytes = value;
+            break;
+        case AR_Q_DEVICE_STATUS:
+            if (value != 0) return AR_ERR_INVALID_ARG;
+            if (cudaMemset(c.dev_status, 0, 64) != cudaSuccess) return AR_ERR_CUDA;
             break;
         default: return AR_ERR_INVALID_ARG;
     }

@@ -17,6 +17,7 @@ struct VecKernels {
 };
 
 using ExKernelFn = void (*)(ArExParams);
+using TmaKernelFn = void (*)(ArParams, TmaPlan);
 using PackKernelFn = void (*)(const void *, void *, unsigned long long);
 
 struct Kernels {
@@ -29,6 +30,7 @@ struct Kernels {
     int wide_bytes;    // 32 or 16
     KernelFn scalar[2];  // [NC]
     KernelFn naive;
+    TmaKernelFn tma;     // shared-memory staging with bulk copies
 };
 
 // Defined in ar_kernels_f32.cu / ar_kernels_f16.cu / ar_kernels_bf16.cu.
@@ -74,6 +76,7 @@ Kernels make_kernels() {
     k.scalar[0] = ar_scalar_kernel<Td, Tw, false>;
     k.scalar[1] = ar_scalar_kernel<Td, Tw, true>;
     k.naive = ar_naive_kernel<Td, Tw>;
+    k.tma = ar_tma_kernel<Td, Tw>;
     return k;
 }
 

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 TYPES = ["f32", "f16", "bf16"]
 PAIRS = list(itertools.product(TYPES, TYPES))
-VARIANTS = ["auto", "latency", "bandwidth", "scalar", "naive"]
+VARIANTS = ["auto", "latency", "bandwidth", "scalar", "naive", "tma"]
 
 
 @pytest.fixture(scope="module")
@@ -425,7 +425,7 @@ def test_kernel_casts_exhaustive(ctx, wire):
             assert_same(h_out.numpy(), exp, "f32", f"{wire} chunk {start:#x}")
 
 
-@pytest.mark.parametrize("variant", ["auto", "bandwidth", "latency", "scalar"])
+@pytest.mark.parametrize("variant", ["auto", "bandwidth", "latency", "scalar", "tma"])
 def test_sixteen_ranks_sixteen_destinations(ctx, variant):
     """The largest call the ABI allows: R = 16 and n_dsts = 16."""
     n = 65_539
@@ -462,3 +462,46 @@ def test_more_than_2_31_elements(ctx):
     got = out.view(torch.int16)[torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
     exp = oracle.reduce([a[idx], b[idx]], 1, "bf16", "f16")[0]
     assert_same(got, exp, "bf16", "2^31 + 7 elements")
+
+
+@pytest.mark.parametrize("grid", [1, 3, 152])
+def test_tma_grids_and_status(ctx, grid):
+    """The bulk-copy variant on 1, 3 and 152 CTAs (many tiles per CTA, all
+    three stages cycling) gives the oracle's bits, and none of its bounded
+    waits ran out."""
+    tps.ar_init(3, 1 << 20)
+    ctx.R = None
+    tps.ar_set_option("device_status", 0)
+    n = 3_000_017
+    srcs = srcs_for(grid + 500, 3, n, "f32")
+    outs, backs = run(ctx, srcs, 2, "f32", "bf16", variant="tma", grid=grid, pad=64)
+    exp = expect(srcs, "f32", "bf16")
+    for o in outs:
+        assert_same(o, exp, "f32", f"tma grid={grid}")
+    check_guards(backs)
+    assert tps.ar_query("device_status") == 0
+
+
+@pytest.mark.parametrize("stages,tile,ctas", [(2, 1024, 1), (8, 1024, 4), (4, 32768, 1)])
+def test_tma_knobs(ctx, monkeypatch, stages, tile, ctas):
+    """The bulk-copy variant at the edges of its settings (read at ar_init)."""
+    monkeypatch.setenv("AR_TMA_STAGES", str(stages))
+    monkeypatch.setenv("AR_TMA_TILE", str(tile))
+    monkeypatch.setenv("AR_TMA_CTAS_PER_SM", str(ctas))
+    n, R = 1_234_567, 4
+    tps.ar_init(R, n)
+    ctx.R = None
+    try:
+        tps.ar_set_option("device_status", 0)
+        srcs = srcs_for(stages * 100 + ctas, R, n, "bf16")
+        src_t = [to_device(s, "bf16") for s in srcs]
+        dst_t = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        tps.ar_reduce_variant(src_t, dst_t, "tma", nelem=n, dst_dtype="bf16", wire_dtype="f32")
+        torch.cuda.synchronize()
+        exp = expect(srcs, "bf16", "f32")
+        for d in dst_t:
+            assert_same(to_host(d, "bf16"), exp, "bf16", f"tma stages={stages} tile={tile} ctas={ctas}")
+        assert tps.ar_query("device_status") == 0
+    finally:
+        monkeypatch.undo()
+        tps.ar_init(R, n)
