@@ -26,7 +26,7 @@ namespace {
 constexpr int kLatencyThreads = 128;
 constexpr int kBandwidthThreads = 256;
 constexpr int kScalarThreads = 256;
-constexpr int64_t kDefaultLatencyMaxBytes = 4ll << 20;
+constexpr int64_t kDefaultLatencyMaxBytes = 32ll << 20;  // measured crossover on GB300
 // ar_reduce_host cuts a call into chunks of this many bytes per buffer (at
 // most kMaxHostChunks chunks) so that host->device copies, kernels and
 // device->host copies of different chunks overlap.

@@ -395,32 +395,25 @@ struct ArExParams {
     int n_dsts;
 };
 
+// Operand r of element i of row `row`, rounded through the wire type; +0
+// for an inactive rank (the reduction of a zeroed partial).
+template <int Td, int Tw>
+__device__ __forceinline__ float ex_operand(const ArExParams &p, int r, size_t row, size_t i) {
+    if ((p.inactive >> r) & 1u) return 0.0f;
+    const char *base = static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
+    return wire1<Td, Tw>(load_elem<Td, false>(base, i));
+}
+
+// One element of a row, rank after rank (row tails and unaligned layouts;
+// kept sequential so the vector path's register budget is not raised).
 template <int Td, int Tw, bool RES>
 __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, size_t i) {
-    // all loads first (inactive ranks are +0 and not loaded), then the fold
-    float v[kMaxRanks];
-#pragma unroll
-    for (int r = 0; r < kMaxRanks; ++r) {
-        if (r < p.R) {
-            if ((p.inactive >> r) & 1u) {
-                v[r] = 0.0f;
-            } else {
-                const char *base =
-                    static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
-                v[r] = load_elem<Td, false>(base, i);
-            }
-        }
-    }
-    float res = 0.0f;
+    float acc = ex_operand<Td, Tw>(p, 0, row, i);
+    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, ex_operand<Td, Tw>(p, r, row, i));
     if constexpr (RES) {
         const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
-        res = load_elem<Td, false>(rb, i);
+        acc = __fadd_rn(acc, load_elem<Td, false>(rb, i));
     }
-    float acc = wire1<Td, Tw>(v[0]);
-#pragma unroll
-    for (int r = 1; r < kMaxRanks; ++r)
-        if (r < p.R) acc = __fadd_rn(acc, wire1<Td, Tw>(v[r]));
-    if constexpr (RES) acc = __fadd_rn(acc, res);
     for (int d = 0; d < p.n_dsts; ++d)
         store_elem<Td>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d], i, acc);
 }
