@@ -559,6 +559,11 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
         if (!h_srcs[r]) return AR_ERR_INVALID_ARG;
     for (int d = 0; d < n_dsts; ++d)
         if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
+    {  // the launch below checks the device too, but only after copies would be queued
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+        if (dev != c.device) return AR_ERR_INVALID_ARG;
+    }
     if (c.fault_inject) return AR_ERR_CUDA;
 
     // Chunks of whole 256-element groups (so every chunk keeps the buffers'
