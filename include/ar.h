@@ -175,9 +175,14 @@ typedef enum {
                                    persistent grid of n CTAs per SM (capped by occupancy) */
     AR_Q_HOST_CHUNK_BYTES = 9,  /* ar_reduce_host pipeline chunk, bytes per buffer (default 4 MiB;
                                    at most 64 chunks per call) */
-    AR_Q_DEVICE_STATUS = 10     /* device-side status word (bit 0: a bounded wait of the TMA
+    AR_Q_DEVICE_STATUS = 10,    /* device-side status word (bit 0: a bounded wait of the TMA
                                    variant ran out); reading it synchronises with the device;
                                    set it to 0 to clear it */
+    AR_Q_TMA_DROP_TILE = 11     /* test hook for failure detection, -1 (default) = off: TMA
+                                   launches never load tile n, so the CTA that owns it waits
+                                   for data that never comes until its bound (100 ms) runs out,
+                                   reports through AR_Q_DEVICE_STATUS and returns; the results of
+                                   such a launch are unspecified and the context stays usable */
 } ar_key;
 
 /* Read one context value into *value.  AR_ERR_NOT_INITIALIZED before init. */

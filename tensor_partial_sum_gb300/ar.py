@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "AR_OK", 1: "AR_ERR_INVALID_ARG", 2: "AR_ERR_UNSUPPORTED", 3:
 VARIANTS = {"auto": 0, "naive": 1, "latency": 2, "bandwidth": 3, "scalar": 4, "tma": 5}
 KEYS = {"ranks": 0, "max_elems": 1, "device": 2, "sm_count": 3, "latency_max_bytes": 4,
         "forced_variant": 5, "last_variant": 6, "fault_inject": 7, "bw_blocks_per_sm": 8,
-        "host_chunk_bytes": 9, "device_status": 10}
+        "host_chunk_bytes": 9, "device_status": 10, "tma_drop_tile": 11}
 
 _lib = None
 

@@ -58,6 +58,7 @@ struct Context {
     int tma_stages = 3;              // AR_TMA_STAGES (2..8)
     int tma_tile = 16384;            // AR_TMA_TILE: largest tile, bytes (1024 .. 32768, 1 KiB multiples)
     int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
+    int64_t tma_drop_tile = -1;      // test hook (AR_Q_TMA_DROP_TILE), -1 = off
 };
 
 void destroy_pipe(HostPipe &p) {
@@ -175,6 +176,7 @@ int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t 
     plan.ntiles = (plan.vec_bytes + tile - 1) / tile;
     plan.status = c.dev_status;
     plan.timeout_ns = 100ull * 1000 * 1000;
+    plan.drop_tile = c.tma_drop_tile < 0 ? ~0ull : static_cast<unsigned long long>(c.tma_drop_tile);
     const size_t smem = tps::kTmaHeaderBytes + (S * p.R + 2) * tile;
     if (cudaFuncSetAttribute(reinterpret_cast<const void *>(k.tma), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
@@ -500,6 +502,7 @@ int ar_query(int key, int64_t *value) {
         case AR_Q_FAULT_INJECT: *value = c.fault_inject; break;
         case AR_Q_BW_BLOCKS_PER_SM: *value = c.bw_blocks_per_sm; break;
         case AR_Q_HOST_CHUNK_BYTES: *value = c.host_chunk_bytes; break;
+        case AR_Q_TMA_DROP_TILE: *value = c.tma_drop_tile; break;
         case AR_Q_DEVICE_STATUS: {
             unsigned v = 0;
             if (cudaMemcpy(&v, c.dev_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return AR_ERR_CUDA;
@@ -532,6 +535,10 @@ int ar_set_option(int key, int64_t value) {
         case AR_Q_HOST_CHUNK_BYTES:
             if (value < 1) return AR_ERR_INVALID_ARG;
             c.host_chunk_bytes = value;
+            break;
+        case AR_Q_TMA_DROP_TILE:
+            if (value < -1) return AR_ERR_INVALID_ARG;
+            c.tma_drop_tile = value;
             break;
         case AR_Q_DEVICE_STATUS:
             if (value != 0) return AR_ERR_INVALID_ARG;

@@ -564,6 +564,7 @@ struct TmaPlan {
     unsigned stages;               // 2 .. kTmaMaxStages
     unsigned *status;              // device word: bit 0 = a wait timed out
     unsigned long long timeout_ns; // bound of every wait
+    unsigned long long drop_tile;  // test hook: this tile's loads are never issued (~0 = none)
 };
 
 constexpr int kTmaMaxStages = 8;
@@ -677,10 +678,12 @@ __global__ void __launch_bounds__(kTmaThreads) ar_tma_kernel(const __grid_consta
                 if (*abort_flag) break;
                 const unsigned long long off = (blockIdx.x + k * G) * T;
                 const unsigned bytes = static_cast<unsigned>(min(static_cast<unsigned long long>(T), plan.vec_bytes - off));
-                mbar_expect_tx(&full[s], bytes * p.R);
-                for (int r = 0; r < p.R; ++r)
-                    bulk_load(in + (static_cast<size_t>(s) * p.R + r) * T, static_cast<const char *>(p.src[r]) + off,
-                              bytes, &full[s]);
+                if (blockIdx.x + k * G != plan.drop_tile) {  // the hook leaves the stage's barrier waiting
+                    mbar_expect_tx(&full[s], bytes * p.R);
+                    for (int r = 0; r < p.R; ++r)
+                        bulk_load(in + (static_cast<size_t>(s) * p.R + r) * T,
+                                  static_cast<const char *>(p.src[r]) + off, bytes, &full[s]);
+                }
                 issued = k + 1;
             }
             // before leaving, every copy this warp started must have landed

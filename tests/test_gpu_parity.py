@@ -505,3 +505,29 @@ def test_tma_knobs(ctx, monkeypatch, stages, tile, ctas):
     finally:
         monkeypatch.undo()
         tps.ar_init(R, n)
+
+
+def test_tma_bounded_wait_runs_out_reports_and_context_survives(ctx):
+    """Failure detection without a GPU fault: the test hook keeps one tile's
+    data from ever arriving, the waiting CTA gives up after its bound,
+    the host reads the error from the status word, and the same context
+    then reduces correctly again."""
+    R, n = 2, 1_000_003
+    tps.ar_init(R, n)
+    ctx.R = None
+    srcs = srcs_for(777, R, n, "f32")
+    src_t = [to_device(s, "f32") for s in srcs]
+    out = torch.empty(n, device="cuda")
+    tps.ar_set_option("device_status", 0)
+    tps.ar_set_option("tma_drop_tile", 3)
+    try:
+        tps.ar_reduce_variant(src_t, [out], "tma", dst_dtype="f32", wire_dtype="bf16")
+        torch.cuda.synchronize()  # ends: the wait is bounded
+        assert tps.ar_query("device_status") & 1
+    finally:
+        tps.ar_set_option("tma_drop_tile", -1)
+    tps.ar_set_option("device_status", 0)
+    tps.ar_reduce_variant(src_t, [out], "tma", dst_dtype="f32", wire_dtype="bf16")
+    torch.cuda.synchronize()
+    assert tps.ar_query("device_status") == 0
+    assert_same(to_host(out, "f32"), expect(srcs, "f32", "bf16"), "f32", "after a timed-out launch")
