@@ -34,11 +34,9 @@ METRIC = "effective HBM GB/s (% of roofline) prefill-size; µs/call decode-size"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ar_reduce_kernel_prefill_traffic.md")
-# the device code and its instantiations: the traffic of a launch depends on these, not on
-# the host code around them
-KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", f)
-                  for f in ("ar_kernels.cuh", "ar_dispatch.h", "ar_kernels_f32.cu", "ar_kernels_f16.cu",
-                            "ar_kernels_bf16.cu")]
+# the file that defines the timed kernel (ar_reduce_kernel) and its helpers: a launch's
+# traffic depends on this code, not on the host code or the other kernels
+KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", "ar_kernels.cuh")]
 
 
 # ---- distributed plumbing (also exercised by the CPU tests with gloo) -------

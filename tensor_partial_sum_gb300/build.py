@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libtps_ar.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("ar.cu", "ar_kernels_f32.cu", "ar_kernels_f16.cu", "ar_kernels_bf16.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ar_kernels.cuh", "ar_dispatch.h")] + [os.path.join(INCLUDE, "ar.h")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ar_kernels.cuh", "ar_kernels_ex.cuh", "ar_kernels_tma.cuh",
+                                                   "ar_dispatch.h")] + [os.path.join(INCLUDE, "ar.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -3,6 +3,8 @@
 #pragma once
 
 #include "ar_kernels.cuh"
+#include "ar_kernels_ex.cuh"
+#include "ar_kernels_tma.cuh"
 
 namespace tps {
 

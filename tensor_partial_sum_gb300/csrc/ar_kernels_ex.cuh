@@ -1,0 +1,176 @@
+// Device code of the extended entry points: ar_reduce_ex (row strides,
+// inactive ranks, residual / bias) and ar_wire_pack.  Built on the casts and
+// element helpers of ar_kernels.cuh.
+#pragma once
+
+#include "ar_kernels.cuh"
+
+// ==== extended layouts: row strides, inactive ranks, residual / bias ======
+namespace tps {
+
+// Kernel arguments of ar_reduce_ex_kernel (by value, about 560 bytes).
+struct ArExParams {
+    const void *src[kMaxRanks];
+    void *dst[kMaxDsts];
+    long long src_stride[kMaxRanks];  // row strides in bytes
+    long long dst_stride[kMaxDsts];
+    const void *residual;             // nullptr: none
+    long long res_stride;             // 0: one row broadcast to every row
+    unsigned long long ne0;           // elements per row
+    unsigned long long ne1;           // rows
+    unsigned inactive;                // bit r: rank r contributes +0
+    int R;
+    int n_dsts;
+};
+
+// Operand r of element i of row `row`, rounded through the wire type; +0
+// for an inactive rank (the reduction of a zeroed partial).
+template <int Td, int Tw>
+__device__ __forceinline__ float ex_operand(const ArExParams &p, int r, size_t row, size_t i) {
+    if ((p.inactive >> r) & 1u) return 0.0f;
+    const char *base = static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
+    return wire1<Td, Tw>(load_elem<Td, false>(base, i));
+}
+
+// One element of a row, rank after rank (row tails and unaligned layouts;
+// kept sequential so the vector path's register budget is not raised).
+template <int Td, int Tw, bool RES>
+__device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, size_t i) {
+    float acc = ex_operand<Td, Tw>(p, 0, row, i);
+    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, ex_operand<Td, Tw>(p, r, row, i));
+    if constexpr (RES) {
+        const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
+        acc = __fadd_rn(acc, load_elem<Td, false>(rb, i));
+    }
+    for (int d = 0; d < p.n_dsts; ++d)
+        store_elem<Td>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d], i, acc);
+}
+
+// Reduction over ne1 rows of ne0 elements.  blockIdx.y strides over rows;
+// within a row, thread t of CTA x owns VB-byte vector x*blockDim.x + t,
+// loading RB ranks at a time (inactive ranks are not loaded: their operand
+// is +0), then adds the residual (not rounded through the wire type) after
+// the rank fold, casts once and stores to every destination.  The last CTA
+// in x does the row's tail of fewer than one vector, element by element.
+// VEC = false runs every element through that element-wise path (buffers
+// or strides not 16-byte aligned).
+template <int Td, int Tw, int RB, bool RES, bool VEC, int VB = 16>
+__global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant__ ArExParams p) {
+    constexpr int NW = VB / 4;
+    constexpr int V = VB / Elem<Td>::bytes;
+    const size_t vpr = VEC ? p.ne0 / V : 0;  // whole vectors per row
+    const size_t tail0 = vpr * V;
+    for (size_t row = blockIdx.y; row < p.ne1; row += gridDim.y) {
+        if constexpr (VEC) {
+            const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+            if (v < vpr) {
+                float acc[V];
+                for (int r0 = 0; r0 < p.R; r0 += RB) {
+                    uint32_t w[RB][NW];
+#pragma unroll
+                    for (int j = 0; j < RB; ++j) {
+                        const int r = r0 + j;
+                        if (r < p.R && !((p.inactive >> r) & 1u)) {
+                            const char *base = static_cast<const char *>(p.src[r]) +
+                                               static_cast<long long>(row) * p.src_stride[r] + v * VB;
+                            load_words<VB, false>(base, w[j]);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < NW; ++k) w[j][k] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < RB; ++j) {
+                        if (r0 + j < p.R) {
+                            float x[V];
+                            word_operands<Td, Tw, NW>(w[j], x);
+#pragma unroll
+                            for (int k = 0; k < V; ++k) acc[k] = (r0 + j == 0) ? x[k] : __fadd_rn(acc[k], x[k]);
+                        }
+                    }
+                }
+                if constexpr (RES) {
+                    uint32_t rw[NW];
+                    load_words<VB, false>(static_cast<const char *>(p.residual) +
+                                              static_cast<long long>(row) * p.res_stride + v * VB,
+                                          rw);
+                    float x[V];
+                    word_operands<Td, Td, NW>(rw, x);  // widened, no wire rounding
+#pragma unroll
+                    for (int k = 0; k < V; ++k) acc[k] = __fadd_rn(acc[k], x[k]);
+                }
+                uint32_t out[NW];
+                word_pack<Td, NW>(acc, out);
+                for (int d = 0; d < p.n_dsts; ++d)
+                    store_words<VB>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d] +
+                                        v * VB,
+                                    out);
+            }
+            if (blockIdx.x == gridDim.x - 1) {
+                const size_t i = tail0 + threadIdx.x;
+                if (i < p.ne0) ex_reduce_elem<Td, Tw, RES>(p, row, i);
+            }
+        } else {
+            for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.ne0;
+                 i += static_cast<size_t>(gridDim.x) * blockDim.x)
+                ex_reduce_elem<Td, Tw, RES>(p, row, i);
+        }
+    }
+}
+
+// Wire pack: wire[i] = T_wire(value(src[i])), the buffer a transport would
+// send (phase 1 of ggml_cuda_ar_kernel in ggml-cuda allreduce.cu).  VEC:
+// each thread converts one VB-byte vector of sources (16 or 32 bytes); the
+// last CTA does the tail element by element.
+template <int Td, int Tw, bool VEC, int VB = 16>
+__global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem) {
+    constexpr int NW = VB / 4;
+    constexpr int V = VB / Elem<Td>::bytes;
+    constexpr int WB = V * Elem<Tw>::bytes;  // output bytes per vector: 8, 16 or 32
+    auto one = [&](size_t i) {
+        float a = load_elem<Td, false>(src, i);
+        if constexpr (Tw == kF32) {
+            static_cast<float *>(wire)[i] = a;
+        } else {
+            float b = a;
+            static_cast<unsigned short *>(wire)[i] = static_cast<unsigned short>(narrow2<Tw>(a, b) & 0xFFFFu);
+        }
+    };
+    if constexpr (VEC) {
+        const size_t nvec = nelem / V;
+        const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (v < nvec) {
+            uint32_t w[NW];
+            load_words<VB, false>(static_cast<const char *>(src) + v * VB, w);  // may run in place
+            float x[V];
+            word_operands<Td, Td, NW>(w, x);  // exact values
+            char *o = static_cast<char *>(wire) + v * WB;
+            constexpr int OW = WB / 4;  // output words: 2, 4 or 8
+            uint32_t ow[OW];
+            if constexpr (Tw == kF32) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) ow[k] = __float_as_uint(x[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V / 2; ++k) ow[k] = narrow2<Tw>(x[2 * k], x[2 * k + 1]);
+            }
+            if constexpr (OW == 2) {
+                asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(o), "r"(ow[0]), "r"(ow[1]) : "memory");
+            } else if constexpr (OW == 4) {
+                store_words<16>(o, reinterpret_cast<uint32_t(&)[4]>(ow));
+            } else {
+                store_words<32>(o, reinterpret_cast<uint32_t(&)[8]>(ow));
+            }
+        }
+        if (blockIdx.x == gridDim.x - 1) {
+            const size_t i = nvec * V + threadIdx.x;
+            if (i < nelem) one(i);
+        }
+    } else {
+        for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nelem;
+             i += static_cast<size_t>(gridDim.x) * blockDim.x)
+            one(i);
+    }
+}
+
+}  // namespace tps
