@@ -132,11 +132,20 @@ def _stream(s) -> int | None:
 
 
 def _infer(srcs, nelem, dst_dtype):
+    """nelem and dtype code from the first buffer unless given: torch tensors
+    and numpy arrays (float32 -> f32, float16 -> f16; uint16 bit patterns are
+    ambiguous between f16 and bf16 and need an explicit dst_dtype)."""
     t = srcs[0] if srcs else None
     if nelem is None:
-        nelem = t.numel()
+        nelem = t.numel() if hasattr(t, "numel") else int(t.size)
     if dst_dtype is None:
-        dst_dtype = t.dtype
+        if hasattr(t, "numel"):
+            dst_dtype = t.dtype
+        else:
+            name = {"float32": "f32", "float16": "f16"}.get(str(t.dtype))
+            if name is None:
+                raise TypeError(f"cannot tell the element type of a {t.dtype} array: pass dst_dtype")
+            dst_dtype = name
     return nelem, _dtype_code(dst_dtype)
 
 
