@@ -7,9 +7,11 @@
 // ggml_cuda_ar_pipeline_free) without the transport: on one GPU the R
 // partials are plain device buffers, so a call is one kernel launch on the
 // caller's stream.  ggml_cuda_ar_allreduce chooses its strategy by byte
-// count; here the choice is between a one-shot latency launch and a
-// persistent bandwidth grid.  Status codes instead of asserts follow
-// validate_allreduce / op_allreduce in ggml-hexagon htp/allreduce-ops.c.
+// count; here the byte count chooses the launch shape of one kernel family:
+// 16-byte vectors in 128-thread blocks below the switch, the widest aligned
+// vectors in 256-thread blocks above it.  Status codes instead of asserts
+// follow validate_allreduce / op_allreduce in ggml-hexagon
+// htp/allreduce-ops.c.
 #include "ar.h"
 
 #include <cstdio>
