@@ -20,6 +20,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -85,11 +86,19 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_tokens(text: str) -> str:
+    """Source text without comments and with whitespace collapsed: what the
+    compiler sees, so editing a comment does not count as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_digest() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

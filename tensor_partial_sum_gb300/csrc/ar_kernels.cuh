@@ -25,7 +25,7 @@ constexpr int kBF16 = 2;
 constexpr int kMaxRanks = 16;
 constexpr int kMaxDsts = 16;
 
-// Kernel arguments, passed by value (272 bytes) as a __grid_constant__.
+// Kernel arguments, passed by value (288 bytes) as a __grid_constant__.
 struct ArParams {
     const void *src[kMaxRanks];
     void *dst[kMaxDsts];
@@ -258,7 +258,7 @@ __device__ __forceinline__ void word_pack(const float (&acc)[NW * 4 / Elem<Td>::
 }
 
 // The vectors [first, end) of one thread block, RB ranks per batch, U
-// vectors per thread per tile; see ar_bw_kernel.
+// vectors per thread per tile; see ar_reduce_kernel.
 template <int Td, int Tw, int VB, int U, int RB, bool NC>
 __device__ __forceinline__ void reduce_span(const ArParams &p, size_t first, size_t end) {
     constexpr int NW = VB / 4;

@@ -47,3 +47,10 @@ def test_traffic_field_follows_the_kernel_sources():
 
 def test_aggregate():
     assert bench.aggregate_gbs(134217728, 100, 2, 0.001) == 2 * 134217728 * 100 / 0.001 / 1e9
+
+
+def test_digest_ignores_comments_and_whitespace():
+    a = "int f(int x) { // add one\n  return x + 1; /* done */ }\n"
+    b = "int f(int x) {\n\n    return x + 1;   }"
+    assert bench.code_tokens(a) == bench.code_tokens(b)
+    assert bench.code_tokens(a) != bench.code_tokens(a.replace("x + 1", "x + 2"))
