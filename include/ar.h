@@ -81,19 +81,24 @@ typedef enum {
 #define AR_MAX_DSTS 16
 
 /* Kernel variants.  AUTO picks LATENCY or BANDWIDTH by the call's byte
- * count (and SCALAR when a pointer is not 16-byte aligned).  Every variant
- * computes the same bits. */
+ * count.  The vector variants want every source and destination at the same
+ * offset from a 16-byte boundary (32 for BANDWIDTH's wide f32 vectors, else
+ * 16): they then shift past the few elements before the boundary, which they
+ * reduce one by one.  When the offsets differ AUTO takes SCALAR.  Every
+ * variant computes the same bits. */
 typedef enum {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_NAIVE = 1,     /* one element per thread, grid-stride: a cross-check */
     AR_VARIANT_LATENCY = 2,   /* one 16-byte vector per thread, 128-thread CTAs */
     AR_VARIANT_BANDWIDTH = 3, /* one 32-byte (f32) or 16-byte vector per thread, 256-thread
                                  CTAs; all loads of two or four ranks issued together */
-    AR_VARIANT_SCALAR = 4,    /* element-wise path used for unaligned pointers */
+    AR_VARIANT_SCALAR = 4,    /* element-wise path used when the buffers' offsets differ */
     AR_VARIANT_TMA = 5        /* shared-memory staging: a producer warp bulk-copies (cp.async.bulk)
                                  R source tiles per stage, eight warps fold them, one thread
                                  bulk-stores the result tile to every destination; one CTA per SM.
-                                 Never chosen by AUTO.  Its internal waits are bounded: a wait
+                                 Needs 16-byte aligned buffers.  Never chosen by AUTO (an
+                                 AR_VARIANT environment override with offset buffers takes
+                                 BANDWIDTH, or SCALAR when the offsets differ).  Its internal waits are bounded: a wait
                                  that runs out sets bit 0 of AR_Q_DEVICE_STATUS and the call's
                                  results are then unspecified (the call still ends). */
 } ar_variant;
@@ -126,8 +131,8 @@ int ar_init(int R, size_t max_elems);
  *   dst_dtype  ar_dtype of sources and destinations.
  *   wire_dtype ar_dtype every operand is rounded through (any of the three).
  *   stream     CUDA stream of the init device (0 = legacy default stream).
- * Any element-aligned pointer works; 16-byte-aligned pointers take the
- * vector paths.  Returns an ar_status.
+ * Any element-aligned pointer works; buffers that all share one offset from
+ * a 16-byte boundary take the vector paths.  Returns an ar_status.
  */
 int ar_reduce(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem,
               int dst_dtype, int wire_dtype, cudaStream_t stream);
@@ -153,8 +158,9 @@ int ar_check_args(int R, const void *const *srcs, void *const *dsts, int n_dsts,
  *               choice); ignored by LATENCY, whose grid covers the tensor.
  *               A BANDWIDTH grid smaller than the tensor needs is persistent:
  *               its CTAs sweep the tensors together in rounds.
- * The result bits do not depend on either argument.  A vector variant asked
- * for with unaligned pointers returns AR_ERR_INVALID_ARG.
+ * The result bits do not depend on either argument.  LATENCY or BANDWIDTH
+ * asked for with buffers at different offsets from a 16-byte boundary, or
+ * TMA with any buffer off that boundary, returns AR_ERR_INVALID_ARG.
  */
 int ar_reduce_variant(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem,
                       int dst_dtype, int wire_dtype, int variant, int grid_blocks,

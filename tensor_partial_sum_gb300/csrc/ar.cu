@@ -202,15 +202,23 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
     if (dev != c.device) return AR_ERR_INVALID_ARG;
 
-    uintptr_t any_bits = 0;  // OR of all addresses: its low bits give the common alignment
     bool alias = false;
-    for (int r = 0; r < c.R; ++r) any_bits |= reinterpret_cast<uintptr_t>(srcs[r]);
-    for (int d = 0; d < n_dsts; ++d) {
-        any_bits |= reinterpret_cast<uintptr_t>(dsts[d]);
+    for (int d = 0; d < n_dsts; ++d)
         for (int r = 0; r < c.R; ++r) alias |= (dsts[d] == srcs[r]);
-    }
-    const bool aligned = (any_bits % 16) == 0;
-    const bool aligned32 = (any_bits % 32) == 0;
+    // The offset every buffer has from an M-byte boundary when they all share
+    // one, else -1.  A shared offset lets the vector kernels run on buffers
+    // shifted forward to alignment, with the few elements before handled
+    // one by one (the "head").
+    auto common_offset = [&](uintptr_t M) -> long long {
+        const uintptr_t m0 = reinterpret_cast<uintptr_t>(srcs[0]) % M;
+        for (int r = 1; r < c.R; ++r)
+            if (reinterpret_cast<uintptr_t>(srcs[r]) % M != m0) return -1;
+        for (int d = 0; d < n_dsts; ++d)
+            if (reinterpret_cast<uintptr_t>(dsts[d]) % M != m0) return -1;
+        return static_cast<long long>(m0);
+    };
+    const long long off16 = common_offset(16), off32 = common_offset(32);
+    const bool aligned = off16 >= 0;  // vector paths possible (after a head)
 
     const size_t esize = elem_bytes(dst_dtype);
     if (variant == AR_VARIANT_AUTO) variant = c.forced_variant;
@@ -221,6 +229,11 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     if (!aligned && (variant == AR_VARIANT_LATENCY || variant == AR_VARIANT_BANDWIDTH || variant == AR_VARIANT_TMA)) {
         if (explicit_variant) return AR_ERR_INVALID_ARG;
         variant = AR_VARIANT_SCALAR;
+    }
+    if (variant == AR_VARIANT_TMA && off16 != 0) {
+        // bulk copies need 16-byte starts; a shared offset still suits the vector kernel
+        if (explicit_variant) return AR_ERR_INVALID_ARG;
+        variant = AR_VARIANT_BANDWIDTH;
     }
     if (c.fault_inject) return AR_ERR_CUDA;
 
@@ -240,6 +253,15 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     KernelFn fn = nullptr;
     int threads = 0, grid = 0;
     int plan_vec_bytes = 0;  // vector width of an ar_reduce_kernel launch, 0 for the other kernels
+    // Shift every buffer forward past the head to the vector boundary.
+    auto peel = [&](int vec_bytes, long long offset) {
+        long long head = offset ? (vec_bytes - offset) / static_cast<long long>(esize) : 0;
+        if (head > static_cast<long long>(nelem)) head = static_cast<long long>(nelem);
+        for (int r = 0; r < c.R; ++r) p.src[r] = static_cast<const char *>(srcs[r]) + head * esize;
+        for (int d = 0; d < n_dsts; ++d) p.dst[d] = static_cast<char *>(dsts[d]) + head * esize;
+        p.nelem = nelem - static_cast<size_t>(head);
+        p.head = static_cast<int>(head);
+    };
     switch (variant) {
         case AR_VARIANT_LATENCY: {
             // 16-byte vectors, one per thread, a grid that covers the tensor
@@ -247,26 +269,29 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kLatencyThreads;
             plan_vec_bytes = 16;
+            peel(16, off16);
             const long long V = static_cast<long long>(16 / esize);
-            const long long nv = static_cast<long long>(nelem) / V;
+            const long long nv = static_cast<long long>(p.nelem) / V;
             // with a tail, at most threads - V vectors per CTA, so the last CTA
             // has idle threads for the tail
-            const long long per_cta = (static_cast<long long>(nelem) % V) ? threads - V : threads;
+            const long long per_cta = (static_cast<long long>(p.nelem) % V) ? threads - V : threads;
             grid = grid_cap((nv + per_cta - 1) / per_cta, 0x7FFFFFFFll);
             break;
         }
         case AR_VARIANT_BANDWIDTH: {
-            // the widest vectors every pointer is aligned for, one per thread;
-            // a grid that covers the tensor unless a persistent grid is asked for
-            const bool wide = k.wide_bytes == 32 && aligned32;
+            // the widest vectors the buffers' common offset allows, one per
+            // thread; a grid that covers the tensor unless a persistent grid
+            // is asked for
+            const bool wide = k.wide_bytes == 32 && off32 >= 0;
             const tps::VecKernels &vk = wide ? k.wide : k.v16;
             const int vec_bytes = wide ? k.wide_bytes : 16;
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kBandwidthThreads;
             plan_vec_bytes = vec_bytes;
+            peel(vec_bytes, wide ? off32 : off16);
             const long long V = static_cast<long long>(vec_bytes / esize);
-            const long long nv = static_cast<long long>(nelem) / V;
-            const long long per_cta = (static_cast<long long>(nelem) % V) ? threads - V : threads;
+            const long long nv = static_cast<long long>(p.nelem) / V;
+            const long long per_cta = (static_cast<long long>(p.nelem) % V) ? threads - V : threads;
             const long long full = (nv + per_cta - 1) / per_cta;
             if (grid_blocks > 0) {
                 grid = grid_blocks;
@@ -299,7 +324,7 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
 
     if (plan_vec_bytes > 0) {
         // rounds and chunk of ar_reduce_kernel for this grid (one vector per thread per round)
-        const unsigned long long nv = nelem / (plan_vec_bytes / esize);
+        const unsigned long long nv = p.nelem / (plan_vec_bytes / esize);
         const unsigned long long per_round = static_cast<unsigned long long>(grid) * threads;
         p.rounds = (nv + per_round - 1) / per_round;
         p.chunk = p.rounds ? (nv + p.rounds * grid - 1) / (p.rounds * grid) : 0;

@@ -25,7 +25,7 @@ constexpr int kBF16 = 2;
 constexpr int kMaxRanks = 16;
 constexpr int kMaxDsts = 16;
 
-// Kernel arguments, passed by value (288 bytes) as a __grid_constant__.
+// Kernel arguments, passed by value (296 bytes) as a __grid_constant__.
 struct ArParams {
     const void *src[kMaxRanks];
     void *dst[kMaxDsts];
@@ -36,6 +36,11 @@ struct ArParams {
     unsigned long long rounds;
     int R;
     int n_dsts;
+    // Elements before the (aligned) buffer starts that belong to the call:
+    // when every buffer is misaligned by the same amount, the host shifts the
+    // pointers forward to alignment and the first `head` elements sit at
+    // indices -head .. -1.
+    int head;
 };
 
 // Programmatic dependent launch: when a launch opts in, the next kernel on
@@ -129,7 +134,7 @@ __device__ __forceinline__ void wire2(float &a, float &b) {
 
 // ---- one element at a time ----------------------------------------------
 template <int Td, bool NC>
-__device__ __forceinline__ float load_elem(const void *base, size_t i) {
+__device__ __forceinline__ float load_elem(const void *base, long long i) {
     if constexpr (Td == kF32) {
         const float *p = static_cast<const float *>(base) + i;
         return NC ? __ldg(p) : *p;
@@ -143,7 +148,7 @@ __device__ __forceinline__ float load_elem(const void *base, size_t i) {
 }
 
 template <int Td, int Tw, bool NC>
-__device__ __forceinline__ float elem_operand(const void *base, size_t i) {
+__device__ __forceinline__ float elem_operand(const void *base, long long i) {
     float a = load_elem<Td, NC>(base, i);
     float b = a;
     wire2<Td, Tw>(a, b);
@@ -151,7 +156,7 @@ __device__ __forceinline__ float elem_operand(const void *base, size_t i) {
 }
 
 template <int Td>
-__device__ __forceinline__ void store_elem(void *base, size_t i, float v) {
+__device__ __forceinline__ void store_elem(void *base, long long i, float v) {
     if constexpr (Td == kF32) {
         static_cast<float *>(base)[i] = v;
     } else {
@@ -171,7 +176,7 @@ __device__ __forceinline__ float wire1(float a) {
 // before the first is used, so the element path waits for memory once, not
 // once per rank; then the operands are folded in ascending rank order.
 template <int Td, int Tw, bool NC>
-__device__ __forceinline__ void reduce_elem(const ArParams &p, size_t i) {
+__device__ __forceinline__ void reduce_elem(const ArParams &p, long long i) {
     float v[kMaxRanks];
 #pragma unroll
     for (int r = 0; r < kMaxRanks; ++r)
@@ -323,7 +328,8 @@ __device__ __forceinline__ void reduce_span(const ArParams &p, size_t first, siz
 // issued before the first conversion (RB*U*VB bytes in flight per thread),
 // then the batch's operands are added in ascending rank order.  Each warp
 // access covers 32 adjacent vectors.  The last CTA also does the tail of
-// fewer than one vector's elements, on its highest threads.
+// fewer than one vector's elements, on its highest threads, and CTA 0 the
+// head before an aligned start (see ArParams::head), on its highest threads.
 template <int Td, int Tw, int VB, int U, int RB, bool NC>
 __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ ArParams p) {
     constexpr int V = VB / Elem<Td>::bytes;
@@ -346,7 +352,12 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
         // them without a vector (it does whenever there is a tail), the tail's
         // loads overlap the vectors' instead of following them
         const size_t i = nvec * V + (blockDim.x - 1 - threadIdx.x);
-        if (i < p.nelem) reduce_elem<Td, Tw, NC>(p, i);
+        if (i < p.nelem) reduce_elem<Td, Tw, NC>(p, static_cast<long long>(i));
+    }
+    if (blockIdx.x == 0) {
+        // the head before the aligned start (fewer than one vector)
+        const int k = static_cast<int>(blockDim.x) - 1 - static_cast<int>(threadIdx.x);
+        if (k < p.head) reduce_elem<Td, Tw, NC>(p, -1 - k);
     }
 }
 

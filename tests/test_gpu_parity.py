@@ -100,6 +100,48 @@ def test_unaligned_pointers(ctx, dst):
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("dst", TYPES)
+@pytest.mark.parametrize("off", [1, 2, 3, 4, 5, 7])
+@pytest.mark.parametrize("variant", ["auto", "latency", "bandwidth"])
+@pytest.mark.parametrize("n", [1, 2, 7, 9, 10_001, 300_007])
+def test_common_offset_takes_the_vector_path(ctx, dst, off, variant, n):
+    """Buffers that all sit the same number of elements off a vector
+    boundary run the vector kernel on the aligned part, with the elements
+    before it done one by one: same bits, margins intact, no fall-back to
+    the element-wise kernel."""
+    R = 3
+    srcs = srcs_for(100 + off + n, R, n, dst)
+    exp = expect(srcs, dst, "bf16")
+    outs, backs = run(ctx, srcs, 2, dst, "bf16", variant=variant, src_offsets=[off] * R,
+                      dst_offsets=[off, off], pad=64)
+    for o in outs:
+        assert_same(o, exp, dst, f"common offset {off}")
+    check_guards(backs)
+    want = "latency" if variant == "auto" else variant
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS[want]
+
+
+@pytest.mark.parametrize("variant", ["latency", "bandwidth"])
+def test_common_offset_many_ranks_in_place(ctx, variant):
+    """R = 16 with a shared odd offset, destination 0 one of the sources."""
+    n, R = 123_457, 16
+    srcs = srcs_for(77, R, n, "f32")
+    exp = expect(srcs, "f32", "f16")
+    outs, _ = run(ctx, srcs, 2, "f32", "f16", variant=variant, src_offsets=[3] * R,
+                  dst_offsets=[3, 3], in_place=5)
+    for o in outs:
+        assert_same(o, exp, "f32", "R=16 offset 3 in place")
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS[variant]
+
+
+def test_tma_refuses_an_offset(ctx):
+    """The bulk-copy variant needs 16-byte starts even when the offset is shared."""
+    srcs = srcs_for(78, 2, 4096, "f32")
+    with pytest.raises(tps.ARError) as e:
+        run(ctx, srcs, 1, "f32", "bf16", variant="tma", src_offsets=[1, 1], dst_offsets=[1])
+    assert e.value.status == 1
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("k", [0, 2])
 def test_in_place(ctx, variant, k):
@@ -325,18 +367,22 @@ def test_host_entry_direct(ctx, dst, wire, R, n):
         assert_same(h.numpy().view(np.uint32 if dst == "f32" else np.uint16), exp, dst, "direct host")
 
 
-def test_host_entry_direct_unaligned_and_in_place(ctx):
+@pytest.mark.parametrize("offsets,want", [((1, 1, 1), "latency"), ((1, 2, 3), "scalar")])
+def test_host_entry_direct_unaligned_and_in_place(ctx, offsets, want):
+    """Pinned buffers off 16-byte alignment: one shared offset keeps the
+    vector kernel, different offsets take the element-wise one."""
     R, n = 3, 50_001
     ctx.ensure(R, n)
     srcs = srcs_for(5150, R, n, "f32")
     exp = expect(srcs, "f32", "f16")
-    backs = [torch.empty(n + 1, dtype=torch.float32).pin_memory() for _ in range(R)]
-    h_srcs = [b[1:] for b in backs]  # 4 bytes off 16-byte alignment
+    backs = [torch.empty(n + 4, dtype=torch.float32).pin_memory() for _ in range(R)]
+    assert all(b.data_ptr() % 16 == 0 for b in backs)
+    h_srcs = [b[o:o + n] for b, o in zip(backs, offsets)]  # 4 * o bytes off 16-byte alignment
     for h, s in zip(h_srcs, srcs):
         h.copy_(torch.from_numpy(s))
     tps.ar_reduce_host(h_srcs, [h_srcs[2]], nelem=n, dst_dtype="f32", wire_dtype="f16")
     torch.cuda.synchronize()
-    assert tps.ar_query("last_variant") == tps.ar.VARIANTS["scalar"]
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS[want]
     assert_same(h_srcs[2].numpy(), exp, "f32", "direct, unaligned, in place")
 
 
