@@ -174,7 +174,9 @@ typedef enum {
     AR_Q_SM_COUNT = 3,          /* SMs on that device (query only) */
     AR_Q_LATENCY_MAX_BYTES = 4, /* AUTO uses LATENCY below this many bytes */
     AR_Q_FORCED_VARIANT = 5,    /* variant AUTO resolves to when nonzero */
-    AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only) */
+    AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only); after
+                                   ar_reduce_ex: BANDWIDTH for its vector kernel, SCALAR for
+                                   its element-wise one */
     AR_Q_FAULT_INJECT = 7,      /* nonzero: the next launches fail with AR_ERR_CUDA
                                    before anything is enqueued (host-side test hook) */
     AR_Q_BW_BLOCKS_PER_SM = 8,  /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
@@ -267,7 +269,10 @@ typedef struct {
  * stride: an in-place update such as x = x + allreduce(partials)); any other
  * overlap of the buffers' row spans is AR_ERR_OVERLAP (the check is
  * conservative: interleaved rows that never touch are also refused).
- * 16-byte-aligned buffers and strides take the vector path; any other
+ * When every buffer's start agrees modulo 16 bytes, and (with more than one
+ * row) so does every row stride, every row of every buffer starts at one
+ * common offset from a 16-byte boundary: the vector path runs, reducing each
+ * row's few elements before that boundary one by one.  Any other
  * element-aligned layout works element by element with the same bits.
  * Statuses as for ar_reduce; nothing is enqueued unless AR_OK.
  */

@@ -741,36 +741,66 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     p.R = c.R;
     p.n_dsts = n_dsts;
     p.inactive = L->inactive_mask;
-    uintptr_t bits = 0;  // OR of every address and stride: its low bits give the common alignment
+    // The vector kernels need every row of every buffer to start at one
+    // common offset from an M-byte boundary (the kernel reduces the elements
+    // before it one by one): the start addresses agree modulo M, and so do
+    // the row strides when there is more than one row.
+    uintptr_t addr[tps::kMaxRanks + tps::kMaxDsts + 1], stride[tps::kMaxRanks + tps::kMaxDsts + 1];
+    int nbuf = 0;
+    auto add = [&](const void *a, long long st) {
+        addr[nbuf] = reinterpret_cast<uintptr_t>(a);
+        stride[nbuf++] = static_cast<uintptr_t>(st);
+    };
     for (int r = 0; r < c.R; ++r) {
         if ((L->inactive_mask >> r) & 1u) continue;
         p.src[r] = srcs[r];
         p.src_stride[r] = L->src_row_bytes ? L->src_row_bytes[r] : packed;
-        bits |= reinterpret_cast<uintptr_t>(srcs[r]) | (L->ne1 > 1 ? static_cast<uintptr_t>(p.src_stride[r]) : 0);
+        add(srcs[r], p.src_stride[r]);
     }
     for (int d = 0; d < n_dsts; ++d) {
         p.dst[d] = dsts[d];
         p.dst_stride[d] = L->dst_row_bytes ? L->dst_row_bytes[d] : packed;
-        bits |= reinterpret_cast<uintptr_t>(dsts[d]) | (L->ne1 > 1 ? static_cast<uintptr_t>(p.dst_stride[d]) : 0);
+        add(dsts[d], p.dst_stride[d]);
     }
     if (L->residual) {
         p.residual = L->residual;
         p.res_stride = L->residual_row_bytes;
-        bits |= reinterpret_cast<uintptr_t>(L->residual) |
-                (L->ne1 > 1 ? static_cast<uintptr_t>(L->residual_row_bytes) : 0);
+        add(L->residual, L->residual_row_bytes);
     }
-    const bool vec = bits % 16 == 0;
+    auto common = [&](uintptr_t M) {
+        for (int b = 1; b < nbuf; ++b) {
+            if (addr[b] % M != addr[0] % M) return false;
+            if (L->ne1 > 1 && stride[b] % M != stride[0] % M) return false;
+        }
+        return true;
+    };
+    const bool vec = common(16);
     const tps::Kernels &k = kernels_for(dst_dtype, wire_dtype);
-    const bool vec32 = bits % 32 == 0 && k.ex32[0][0] != nullptr;
+    const bool vec32 = k.ex32[0][0] != nullptr && common(32);
     const tps::ExKernelFn fn =
         vec32 ? k.ex32[c.R > 2][L->residual != nullptr] : k.ex[c.R > 2][L->residual != nullptr][vec];
-    const size_t V = (vec32 ? 32 : 16) / es;
+    const size_t VB = vec32 ? 32 : 16;
+    const size_t V = VB / es;
     int threads = 256;
     long long gx;
     if (vec) {
-        const long long vpr = static_cast<long long>(L->ne0 / V);
-        if (vpr < 256) threads = static_cast<int>(vpr < 32 ? 32 : (vpr + 31) / 32 * 32);
-        gx = (vpr + threads - 1) / threads;
+        // threads per row: one per whole vector, plus, when a row can have a
+        // head or a tail (fewer than V elements each), enough idle ones for
+        // both (the kernel relies on them), with the CTA size that wastes
+        // the fewest threads
+        const bool ragged =
+            L->ne0 % V != 0 || addr[0] % VB != 0 || (L->ne1 > 1 && stride[0] % VB != 0);
+        const long long need = static_cast<long long>(L->ne0 / V) + (ragged ? 2 * static_cast<long long>(V) - 2 : 0);
+        if (need <= 256) {
+            threads = static_cast<int>(need < 32 ? 32 : (need + 31) / 32 * 32);
+        } else if (ragged) {
+            long long best = 0;
+            for (int t = 256; t >= 128; t -= 32) {
+                const long long cover = (need + t - 1) / t * t;
+                if (best == 0 || cover < best) best = cover, threads = t;
+            }
+        }
+        gx = (need + threads - 1) / threads;
     } else {
         gx = (static_cast<long long>(L->ne0) + threads - 1) / threads;
         if (gx > 1024) gx = 1024;
@@ -779,6 +809,7 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
     fn<<<dim3(static_cast<unsigned>(gx), gy), threads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    c.last_variant = vec ? AR_VARIANT_BANDWIDTH : AR_VARIANT_SCALAR;
     return AR_OK;
 }
 

@@ -50,18 +50,30 @@ __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, 
 // within a row, thread t of CTA x owns VB-byte vector x*blockDim.x + t,
 // loading RB ranks at a time (inactive ranks are not loaded: their operand
 // is +0), then adds the residual (not rounded through the wire type) after
-// the rank fold, casts once and stores to every destination.  The last CTA
-// in x does the row's tail of fewer than one vector, element by element.
-// VEC = false runs every element through that element-wise path (buffers
-// or strides not 16-byte aligned).
+// the rank fold, casts once and stores to every destination.  With VEC the
+// host guarantees that in every row all buffers sit at one common offset
+// from a VB-byte boundary (read here from destination 0); the vectors start
+// at the first boundary, and the row's head before it and tail after the
+// last whole vector go element by element to the threads left without a
+// vector, so their loads overlap the vectors' instead of following them.
+// The host launches at least ne0/V + 2V - 2 threads in x, which leaves
+// enough idle ones for any head and tail (fewer than V elements each).
+// VEC = false runs every element through the element-wise path (buffers
+// whose row starts sit at different offsets).
 template <int Td, int Tw, int RB, bool RES, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant__ ArExParams p) {
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
-    const size_t vpr = VEC ? p.ne0 / V : 0;  // whole vectors per row
-    const size_t tail0 = vpr * V;
     for (size_t row = blockIdx.y; row < p.ne1; row += gridDim.y) {
         if constexpr (VEC) {
+            // elements of the row before its first VB-byte boundary
+            const unsigned off = static_cast<unsigned>(
+                (reinterpret_cast<uintptr_t>(p.dst[0]) + static_cast<long long>(row) * p.dst_stride[0]) % VB);
+            size_t h = off ? (VB - off) / Elem<Td>::bytes : 0;
+            if (h > p.ne0) h = p.ne0;
+            const size_t vpr = (p.ne0 - h) / V;  // whole vectors in the row
+            const size_t t = p.ne0 - h - vpr * V;  // tail elements
+            const size_t hb = h * Elem<Td>::bytes;
             const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
             if (v < vpr) {
                 float acc[V];
@@ -72,7 +84,7 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
                         const int r = r0 + j;
                         if (r < p.R && !((p.inactive >> r) & 1u)) {
                             const char *base = static_cast<const char *>(p.src[r]) +
-                                               static_cast<long long>(row) * p.src_stride[r] + v * VB;
+                                               static_cast<long long>(row) * p.src_stride[r] + hb + v * VB;
                             load_words<VB, false>(base, w[j]);
                         } else {
 #pragma unroll
@@ -92,7 +104,7 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
                 if constexpr (RES) {
                     uint32_t rw[NW];
                     load_words<VB, false>(static_cast<const char *>(p.residual) +
-                                              static_cast<long long>(row) * p.res_stride + v * VB,
+                                              static_cast<long long>(row) * p.res_stride + hb + v * VB,
                                           rw);
                     float x[V];
                     word_operands<Td, Td, NW>(rw, x);  // widened, no wire rounding
@@ -103,13 +115,13 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
                 word_pack<Td, NW>(acc, out);
                 for (int d = 0; d < p.n_dsts; ++d)
                     store_words<VB>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d] +
-                                        v * VB,
+                                        hb + v * VB,
                                     out);
             }
-            if (blockIdx.x == gridDim.x - 1) {
-                const size_t i = tail0 + threadIdx.x;
-                if (i < p.ne0) ex_reduce_elem<Td, Tw, RES>(p, row, i);
-            }
+            // the threads after the last vector take the head's elements,
+            // then the tail's
+            const size_t u = v - vpr;
+            if (v >= vpr && u < h + t) ex_reduce_elem<Td, Tw, RES>(p, row, u < h ? u : u + vpr * V);
         } else {
             for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.ne0;
                  i += static_cast<size_t>(gridDim.x) * blockDim.x)

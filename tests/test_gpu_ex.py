@@ -114,8 +114,9 @@ def test_shapes(dst, wire, ne0, ne1):
 @pytest.mark.parametrize("kind", ["aligned", "odd_strides", "odd_start"])
 def test_row_strides(dst, kind):
     """Padded rows (ne0 = 777 leaves a ragged tail in every row): strides
-    that are multiples of 16 bytes take the vector path with a per-row tail,
-    odd strides or an odd start the element-wise path; the padding between
+    that are multiples of 16 bytes take the vector path with a per-row tail
+    (after a per-row head when every buffer starts one element in), strides
+    that differ modulo 16 bytes the element-wise path; the padding between
     rows is never written."""
     ne0, ne1, es = 777, 9, ES[dst]
     V = 16 // es
@@ -239,3 +240,52 @@ def test_wire_pack_unaligned_and_in_place(dst, wire):
         tps.ar_wire_pack(src, src, dst_dtype=dst, wire_dtype=wire)
         torch.cuda.synchronize()
         assert_same(to_host(src.view(TORCH_DTYPE[wire]), wire), exp, wire, "pack in place")
+
+
+@pytest.mark.parametrize("dst", TYPES)
+@pytest.mark.parametrize("case", ["start", "odd_stride", "odd_stride_and_start", "residual", "bias",
+                                  "inactive", "different_strides"])
+def test_common_row_offset_takes_the_vector_path(dst, case):
+    """Rows that all start at one offset from a vector boundary, or whose
+    starts all move by the same odd stride, run the vector kernel with each
+    row's head done element by element: same bits, padding intact.  Strides
+    that differ modulo 16 bytes run element by element."""
+    ne0, ne1, R, es = 1001, 13, 3, ES[dst]
+    V = 16 // es
+    lead, pads, res_pad, kw = 0, [V] * R, None, {}
+    if case == "start":
+        lead = V - 1
+    elif case == "odd_stride":
+        pads = [1] * R
+    elif case == "odd_stride_and_start":
+        pads, lead = [3] * R, 2
+    elif case == "residual":
+        pads, lead, res_pad, kw = [1] * R, 1, 1, dict(residual=True)
+    elif case == "bias":  # a broadcast row needs strides that are multiples of 16 bytes
+        pads, lead, kw = [(V - ne0 % V) % V] * R, 1, dict(residual=True, bias=True)
+    elif case == "inactive":
+        pads, lead, kw = [1] * R, 3, dict(inactive=(0,))
+    else:
+        pads = [1, 2, 3]
+    backs = run_ex(R, ne0, ne1, dst, "bf16", seed=len(case) * 7 + es, src_pad=pads, dst_pad=(pads[0], pads[0]),
+                   lead=lead, n_dsts=2, res_pad=res_pad, **kw)
+    want = "scalar" if case == "different_strides" else "bandwidth"
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS[want]
+    for b in backs:
+        b = b.cpu().numpy()
+        stride = (ne0 + pads[0]) * es
+        assert (b[:lead * es] == 0x5A).all(), "bytes before the first row written"
+        for j in range(ne1 - 1):
+            gap = b[lead * es + j * stride + ne0 * es: lead * es + (j + 1) * stride]
+            assert (gap == 0x5A).all(), "padding written"
+        assert (b[lead * es + (ne1 - 1) * stride + ne0 * es:] == 0x5A).all(), "bytes after the last row written"
+
+
+@pytest.mark.parametrize("wire", TYPES)
+def test_common_row_offset_f32_32_byte_path(wire):
+    """f32 strides that agree modulo 32 bytes (here 1036 floats = 4144 bytes,
+    16 modulo 32) with a start 3 floats off: the 32-byte kernel with a
+    per-row head of 5 or 1 elements."""
+    ne0 = 1030
+    run_ex(2, ne0, 9, "f32", wire, seed=5, src_pad=[6, 6], dst_pad=(6,), lead=3, residual=True, res_pad=6)
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS["bandwidth"]
