@@ -175,8 +175,8 @@ typedef enum {
     AR_Q_LATENCY_MAX_BYTES = 4, /* AUTO uses LATENCY below this many bytes */
     AR_Q_FORCED_VARIANT = 5,    /* variant AUTO resolves to when nonzero */
     AR_Q_LAST_VARIANT = 6,      /* variant the last successful launch used (query only); after
-                                   ar_reduce_ex: BANDWIDTH for its vector kernel, SCALAR for
-                                   its element-wise one */
+                                   ar_reduce_ex or ar_wire_pack: BANDWIDTH for their vector
+                                   kernel, SCALAR for their element-wise one */
     AR_Q_FAULT_INJECT = 7,      /* nonzero: the next launches fail with AR_ERR_CUDA
                                    before anything is enqueued (host-side test hook) */
     AR_Q_BW_BLOCKS_PER_SM = 8,  /* 0: the BANDWIDTH grid covers the tensor (default); n > 0: a
@@ -293,7 +293,10 @@ int ar_check_layout(int R, const void *const *srcs, void *const *dsts, int n_dst
  *   src   nelem elements of dst_dtype (device-accessible).
  *   wire  nelem elements of wire_dtype; may be src itself when both types
  *         have the same size, otherwise must not overlap it.
- * Needs ar_init (nelem <= max_elems).  Statuses as for ar_reduce.
+ * Vector kernel when skipping the same first few elements aligns both
+ * buffers (they are then converted one by one), element-wise otherwise; the
+ * bits are the same.  Needs ar_init (nelem <= max_elems).  Statuses as for
+ * ar_reduce.
  */
 int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int wire_dtype,
                  cudaStream_t stream);

@@ -830,22 +830,37 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     if (dev != c.device) return AR_ERR_INVALID_ARG;
     if (c.fault_inject) return AR_ERR_CUDA;
     const tps::Kernels &k = kernels_for(dst_dtype, wire_dtype);
-    // 32-byte source vectors when both buffers allow them, else 16, else element-wise
-    const bool vec32 = k.pack32 != nullptr && a % 32 == 0 && b % (32 / es * ew) == 0;
+    // 32-byte source vectors when both buffers allow them, else 16, else
+    // element-wise.  A buffer pair off a vector boundary still qualifies when
+    // skipping the same few elements (the head) aligns both.
+    auto head_for = [&](size_t vb) -> long long {  // -1: this vector size does not fit
+        const size_t h = (vb - a % vb) % vb / es;
+        const size_t out_bytes = vb / es * ew;  // wire bytes per source vector
+        const size_t out_align = vb == 32 || out_bytes > 16 ? out_bytes : 16;
+        return (b + h * ew) % out_align == 0 ? static_cast<long long>(h) : -1;
+    };
+    long long head = k.pack32 != nullptr ? head_for(32) : -1;
+    const bool vec32 = head >= 0;
+    if (!vec32) head = head_for(16);
+    const bool vec = head >= 0;
     const size_t V = (vec32 ? 32 : 16) / es;
-    const size_t out_bytes = V * ew;  // wire bytes per source vector
-    const bool vec = vec32 || (a % 16 == 0 && b % (out_bytes > 16 ? out_bytes : 16) == 0);
     const tps::PackKernelFn fn = vec32 ? k.pack32 : k.pack[vec];
     long long grid;
     if (vec) {
+        if (head > static_cast<long long>(nelem)) head = static_cast<long long>(nelem);
+        nelem -= static_cast<size_t>(head);
         grid = (static_cast<long long>(nelem / V) + 255) / 256;
     } else {
+        head = 0;
         grid = (static_cast<long long>(nelem) + 255) / 256;
         if (grid > c.sm_count * 8ll) grid = c.sm_count * 8ll;
     }
     if (grid < 1) grid = 1;
-    fn<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, wire, nelem);
+    const void *s0 = static_cast<const char *>(src) + head * es;
+    void *w0 = static_cast<char *>(wire) + head * ew;
+    fn<<<static_cast<unsigned>(grid), 256, 0, stream>>>(s0, w0, nelem, static_cast<int>(head));
     if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    g_ctx.last_variant = vec ? AR_VARIANT_BANDWIDTH : AR_VARIANT_SCALAR;
     return AR_OK;
 }
 

@@ -133,13 +133,16 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
 // Wire pack: wire[i] = T_wire(value(src[i])), the buffer a transport would
 // send (phase 1 of ggml_cuda_ar_kernel in ggml-cuda allreduce.cu).  VEC:
 // each thread converts one VB-byte vector of sources (16 or 32 bytes); the
-// last CTA does the tail element by element.
+// last CTA does the tail element by element, and CTA 0 the `head` elements
+// at indices -head .. -1 (the host shifts both pointers forward past them
+// when the buffers start off a vector boundary).
 template <int Td, int Tw, bool VEC, int VB = 16>
-__global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem) {
+__global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem,
+                                                      int head) {
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
     constexpr int WB = V * Elem<Tw>::bytes;  // output bytes per vector: 8, 16 or 32
-    auto one = [&](size_t i) {
+    auto one = [&](long long i) {
         float a = load_elem<Td, false>(src, i);
         if constexpr (Tw == kF32) {
             static_cast<float *>(wire)[i] = a;
@@ -176,12 +179,16 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
         }
         if (blockIdx.x == gridDim.x - 1) {
             const size_t i = nvec * V + threadIdx.x;
-            if (i < nelem) one(i);
+            if (i < nelem) one(static_cast<long long>(i));
+        }
+        if (blockIdx.x == 0) {
+            const int k = static_cast<int>(blockDim.x) - 1 - static_cast<int>(threadIdx.x);
+            if (k < head) one(-1 - k);
         }
     } else {
         for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nelem;
              i += static_cast<size_t>(gridDim.x) * blockDim.x)
-            one(i);
+            one(static_cast<long long>(i));
     }
 }
 

@@ -289,3 +289,32 @@ def test_common_row_offset_f32_32_byte_path(wire):
     ne0 = 1030
     run_ex(2, ne0, 9, "f32", wire, seed=5, src_pad=[6, 6], dst_pad=(6,), lead=3, residual=True, res_pad=6)
     assert tps.ar_query("last_variant") == tps.ar.VARIANTS["bandwidth"]
+
+
+@pytest.mark.parametrize("dst,wire", PAIRS)
+@pytest.mark.parametrize("offs", [(1, 1), (3, 3), (1, 2), (2, 1), (5, 7), (0, 1)])
+@pytest.mark.parametrize("n", [1, 6, 70_001])
+def test_wire_pack_offsets(dst, wire, offs, n):
+    """Source and wire buffers starting off a vector boundary: where skipping
+    the same first elements aligns both, the vector kernel runs after an
+    element-wise head, else the element-wise kernel; the bits are the same
+    and nothing outside the wire buffer is written."""
+    so, wo = offs
+    (x,) = srcs_for(n + so * 10 + wo, 1, n, dst)
+    tps.ar_init(1, n)
+    back = torch.zeros(n + so, dtype=TORCH_DTYPE[dst], device="cuda")
+    src = back[so:]
+    src.copy_(to_device(x, dst))
+    out_back = torch.full(((n + wo) * ES[wire] + 64,), 0x5A, dtype=torch.uint8, device="cuda")
+    out = out_back[wo * ES[wire]:(n + wo) * ES[wire]].view(TORCH_DTYPE[wire])
+    tps.ar_wire_pack(src, out, dst_dtype=dst, wire_dtype=wire)
+    torch.cuda.synchronize()
+    assert_same(to_host(out, wire), oracle.wire_pack(x, dst, wire), wire, f"pack offsets {offs}")
+    b = out_back.cpu().numpy()
+    assert (b[:wo * ES[wire]] == 0x5A).all() and (b[(n + wo) * ES[wire]:] == 0x5A).all()
+    # the buffers' addresses decide the kernel: some head aligns both or none does
+    a0, b0 = src.data_ptr(), out.data_ptr()
+    fits = any((a0 + h * ES[dst]) % 16 == 0 and (b0 + h * ES[wire]) % max(16 // ES[dst] * ES[wire], 16) == 0
+               for h in range(16 // ES[dst]))
+    if fits:
+        assert tps.ar_query("last_variant") == tps.ar.VARIANTS["bandwidth"]
