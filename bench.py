@@ -20,6 +20,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -197,44 +198,60 @@ def gpu_id_for(device_index: int) -> str:
 
 # ---- the oracle as CPU baseline ------------------------------------------------
 
-def oracle_step(w, srcs, rows: int, out=None):
-    """The oracle's version of one step over the first `rows` rows."""
+def oracle_step(w, srcs, r0: int, r1: int):
+    """The oracle's version of one step over rows [r0, r1) (its results are
+    new arrays; the call releases the GIL while the C oracle runs)."""
     import oracle
-    n = rows * w.ne0
+    a, b = r0 * w.ne0, r1 * w.ne0
     if w.op == "pack":
-        return oracle.wire_pack(srcs[0][:n], w.dst, w.wire)
+        return oracle.wire_pack(srcs[0][a:b], w.dst, w.wire)
     if w.op == "reduce":
-        return oracle.reduce([s[:n] for s in srcs[:w.R]], w.n_dsts, w.dst, w.wire, out=out)
+        return oracle.reduce([s[a:b] for s in srcs[:w.R]], w.n_dsts, w.dst, w.wire)
     res, res_stride = None, None
     if w.residual == "full":
-        res = srcs[w.R][:n]
+        res = srcs[w.R][a:b]
     elif w.residual == "row":
         res, res_stride = srcs[w.R], 0
-    holes = [None if r in w.inactive else s[:n] for r, s in enumerate(srcs[:w.R])]
-    return oracle.reduce_2d(holes, w.n_dsts, w.dst, w.wire, w.ne0, rows, inactive=w.inactive, residual=res,
+    holes = [None if r in w.inactive else s[a:b] for r, s in enumerate(srcs[:w.R])]
+    return oracle.reduce_2d(holes, w.n_dsts, w.dst, w.wire, w.ne0, r1 - r0, inactive=w.inactive, residual=res,
                             residual_stride=res_stride)
 
 
-def oracle_rate(srcs, w, seconds: float, steps: int = 0):
-    """Time the oracle (single thread, as it stands) on a sample of whole rows
-    of the workload.  With steps == 0 the sample and repetitions are sized to
-    take about `seconds`; otherwise `steps` repetitions of a sample sized to
-    take about seconds / steps each.  Returns (GB/s, elapsed, sample text)."""
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate(srcs, w, seconds: float, steps: int = 0, threads: int = 1):
+    """Time the oracle, as it stands, on a sample of whole rows of the
+    workload; with threads > 1 each pass splits the sample into contiguous
+    row ranges, one per thread (every element is independent, so the bytes
+    are those of one call).  With steps == 0 the sample and repetitions are
+    sized to take about `seconds`; otherwise `steps` repetitions of a sample
+    sized to take about seconds / steps each.  Returns (GB/s, elapsed,
+    sample text)."""
+    from concurrent.futures import ThreadPoolExecutor
     probe_rows = max(1, min(w.ne1, (1 << 16) // w.ne0))
     t = time.perf_counter()
-    oracle_step(w, srcs, probe_rows)
-    per_row = max((time.perf_counter() - t) / probe_rows, 1e-9)
+    oracle_step(w, srcs, 0, probe_rows)
+    per_row = max((time.perf_counter() - t) / probe_rows, 1e-9) / threads
     budget = seconds / steps if steps else seconds
     rows = int(min(w.ne1, max(1, budget / per_row)))
     reps = steps if steps else max(1, int(seconds / (per_row * rows)))
-    t = time.perf_counter()
-    for _ in range(reps):
-        oracle_step(w, srcs, rows)
-    el = time.perf_counter() - t
+    threads = max(1, min(threads, rows))
+    cuts = [rows * k // threads for k in range(threads + 1)]
+    with ThreadPoolExecutor(threads) as pool:
+        t = time.perf_counter()
+        for _ in range(reps):
+            list(pool.map(lambda k: oracle_step(w, srcs, cuts[k], cuts[k + 1]), range(threads)))
+        el = time.perf_counter() - t
     moved = w.bytes_per_call * rows / w.ne1 * reps
     return (moved / el / 1e9, el,
             f"first {rows} of {w.ne1} rows ({rows * w.ne0} of {w.nelem} elements) of the workload, "
-            f"{reps} pass(es), {el:.1f} s")
+            f"{reps} pass(es) on {threads} thread(s), {el:.1f} s")
 
 
 # ---- our arm -----------------------------------------------------------------
@@ -446,9 +463,13 @@ def run_ours(args):
         result["decode"] = bench_decode(dev, stream)
 
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        v, el, sample = oracle_rate(srcs_np, w, args.cpu_seconds)
-        result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": sample}
+        # the oracle on every host core, and on one for reference
+        nt = host_threads()
+        v, el, sample = oracle_rate(srcs_np, w, args.cpu_seconds / 2, threads=nt)
+        v1, _, sample1 = oracle_rate(srcs_np, w, args.cpu_seconds / 2)
+        result["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": nt, "kind": "oracle",
+                                  "sample": sample, "single_thread": {"value": round(v1, 4), "sample": sample1},
+                                  "machine": platform.machine()}
     tps.ar_free()
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -526,15 +547,17 @@ def run_reference(args):
     w = W.WORKLOADS[args.workload]
     srcs = W.generate(w)
     budget = args.ref_seconds
-    # untimed warm-up passes on a small sample, then the timed steps
-    oracle_rate(srcs, w, min(1.0, budget / 10), steps=args.warmup)
-    value, el, text = oracle_rate(srcs, w, budget, steps=args.steps)
+    nt = host_threads()
+    # untimed warm-up passes on a small sample, then the timed steps, on every host core
+    oracle_rate(srcs, w, min(1.0, budget / 10), steps=args.warmup, threads=nt)
+    value, el, text = oracle_rate(srcs, w, budget, steps=args.steps, threads=nt)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.describe()}", "parallelism": "oracle on rank 0 only"},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": text},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": nt, "kind": "oracle", "sample": text,
+                         "machine": platform.machine()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

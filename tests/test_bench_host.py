@@ -54,3 +54,29 @@ def test_digest_ignores_comments_and_whitespace():
     b = "int f(int x) {\n\n    return x + 1;   }"
     assert bench.code_tokens(a) == bench.code_tokens(b)
     assert bench.code_tokens(a) != bench.code_tokens(a.replace("x + 1", "x + 2"))
+
+
+def test_oracle_row_ranges_tile_the_step():
+    """The threaded CPU baseline splits a step into contiguous row ranges:
+    their results, laid end to end, are the whole step's bytes, for every
+    kind of step the workloads have."""
+    import numpy as np
+    from tensor_partial_sum_gb300 import workloads as W
+    for name in ["tp_small", "prefill_bias", "prefill_inactive", "prefill_pack"]:
+        w = W.WORKLOADS[name]
+        srcs = W.generate(w)
+        whole = bench.oracle_step(w, srcs, 0, 40)
+        parts = [bench.oracle_step(w, srcs, a, b) for a, b in [(0, 13), (13, 14), (14, 40)]]
+        if w.op == "pack":
+            assert np.array_equal(whole.view(np.uint8), np.concatenate(parts).view(np.uint8)), name
+        else:
+            for d in range(w.n_dsts):
+                cat = np.concatenate([p[d] for p in parts])
+                assert np.array_equal(whole[d].view(np.uint8), cat.view(np.uint8)), (name, d)
+
+
+def test_oracle_rate_reports_its_threads():
+    from tensor_partial_sum_gb300 import workloads as W
+    w = W.WORKLOADS["tp_small"]
+    v, el, text = bench.oracle_rate(W.generate(w), w, 0.2, steps=2, threads=2)
+    assert v > 0 and el > 0 and "on 2 thread(s)" in text
