@@ -193,7 +193,9 @@ __device__ __forceinline__ void reduce_elem(const ArParams &p, long long i) {
 // ---- words of a wide vector ----------------------------------------------
 // A vector of VB bytes (16 or 32) held as VB/4 32-bit words.  32-byte
 // accesses (ld/st .v8.b32) need 32-byte-aligned addresses and halve the
-// number of memory instructions per byte.
+// number of memory instructions per byte.  NC loads take the non-coherent
+// path, valid only when nothing the kernel writes is read; the others are
+// coherent.  Neither allocates in L1: every byte is read once.
 template <int VB, bool NC>
 __device__ __forceinline__ void load_words(const void *p, uint32_t (&w)[VB / 4]) {
     static_assert(VB == 16 || VB == 32, "vector width");
@@ -203,7 +205,7 @@ __device__ __forceinline__ void load_words(const void *p, uint32_t (&w)[VB / 4])
                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                 : "l"(p));
         } else {
-            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+            asm volatile("ld.global.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                          : "l"(p)
                          : "memory");
@@ -215,7 +217,7 @@ __device__ __forceinline__ void load_words(const void *p, uint32_t (&w)[VB / 4])
                   "=r"(w[7])
                 : "l"(p));
         } else {
-            asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
                            "=r"(w[7])
                          : "l"(p)

@@ -76,6 +76,13 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
             const size_t hb = h * Elem<Td>::bytes;
             const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
             if (v < vpr) {
+                // the residual's load is issued first so that it overlaps the
+                // ranks'; it is still added after the fold
+                uint32_t rw[NW];
+                if constexpr (RES)
+                    load_words<VB, false>(static_cast<const char *>(p.residual) +
+                                              static_cast<long long>(row) * p.res_stride + hb + v * VB,
+                                          rw);
                 float acc[V];
                 for (int r0 = 0; r0 < p.R; r0 += RB) {
                     uint32_t w[RB][NW];
@@ -102,10 +109,6 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
                     }
                 }
                 if constexpr (RES) {
-                    uint32_t rw[NW];
-                    load_words<VB, false>(static_cast<const char *>(p.residual) +
-                                              static_cast<long long>(row) * p.res_stride + hb + v * VB,
-                                          rw);
                     float x[V];
                     word_operands<Td, Td, NW>(rw, x);  // widened, no wire rounding
 #pragma unroll
