@@ -369,14 +369,9 @@ int reduce_host_direct_locked(const void *const *h_srcs, void *const *h_dsts, in
     }
     const int st = ar_check_args(c.R, s, d, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
     if (st != AR_OK || nelem == 0) return st;
-    const bool vector_ok = [&] {
-        uintptr_t bits = 0;
-        for (int r = 0; r < c.R; ++r) bits |= reinterpret_cast<uintptr_t>(s[r]);
-        for (int k = 0; k < n_dsts; ++k) bits |= reinterpret_cast<uintptr_t>(d[k]);
-        return bits % 16 == 0;
-    }();
-    return launch_locked(s, d, n_dsts, nelem, dst_dtype, wire_dtype,
-                         vector_ok ? AR_VARIANT_BANDWIDTH : AR_VARIANT_AUTO, vector_ok ? c.sm_count : 0, stream,
+    // one CTA per SM; buffers at different offsets from a vector boundary
+    // fall back to the element-wise kernel on the same grid
+    return launch_locked(s, d, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_BANDWIDTH, c.sm_count, stream,
                          false);
 }
 
