@@ -113,6 +113,41 @@ def _ptrs(xs):
     return (ctypes.c_void_p * len(ptrs))(*ptrs)
 
 
+ESIZE = {AR_F32: 4, AR_F16: 2, AR_BF16: 2}
+
+
+def _checked(xs, nelem, dcode, where, call):
+    """Check the buffers of a 1-D call before their addresses reach the
+    library: torch tensors and numpy arrays must be contiguous, hold at
+    least ``nelem`` elements of the call's type, and live where the entry
+    point reads them (``where`` = "device" or "host").  Plain integers are
+    addresses the caller vouches for.  A wrong buffer would otherwise be
+    read or written past its end by a kernel."""
+    if xs is None:
+        return xs
+    need = nelem * ESIZE.get(dcode, 1)
+    for k, x in enumerate(xs):
+        if x is None or isinstance(x, int):
+            continue
+        if hasattr(x, "data_ptr"):
+            if (x.device.type == "cuda") != (where == "device"):
+                raise TypeError(f"{call}: buffer {k} is a {x.device.type} tensor, a {where} buffer is needed")
+            if not x.is_contiguous():
+                raise ValueError(f"{call}: buffer {k} is not contiguous")
+            have = x.numel() * x.element_size()
+        elif hasattr(x, "ctypes"):
+            if where != "host":
+                raise TypeError(f"{call}: buffer {k} is a numpy array, a device buffer is needed")
+            if not x.flags["C_CONTIGUOUS"]:
+                raise ValueError(f"{call}: buffer {k} is not contiguous")
+            have = x.nbytes
+        else:
+            continue
+        if have < need:
+            raise ValueError(f"{call}: buffer {k} holds {have} bytes, the call needs {need}")
+    return xs
+
+
 def _dtype_code(d) -> int:
     if isinstance(d, int):
         return d
@@ -174,6 +209,8 @@ def ar_reduce(srcs, dsts, nelem=None, dst_dtype=None, wire_dtype="bf16", stream=
     every tensor of ``dsts``.  ``nelem``/``dst_dtype`` default to the first
     source tensor's; ``stream`` defaults to torch's current stream."""
     nelem, dcode = _infer(srcs, nelem, dst_dtype)
+    _checked(srcs, nelem, dcode, "device", "ar_reduce")
+    _checked(dsts, nelem, dcode, "device", "ar_reduce")
     _check(lib().ar_reduce(_ptrs(srcs), _ptrs(dsts), len(dsts), nelem, dcode, _dtype_code(wire_dtype),
                            _stream(stream)), "ar_reduce")
 
@@ -181,6 +218,8 @@ def ar_reduce(srcs, dsts, nelem=None, dst_dtype=None, wire_dtype="bf16", stream=
 def ar_reduce_variant(srcs, dsts, variant="auto", grid_blocks=0, nelem=None, dst_dtype=None,
                       wire_dtype="bf16", stream=None) -> None:
     nelem, dcode = _infer(srcs, nelem, dst_dtype)
+    _checked(srcs, nelem, dcode, "device", "ar_reduce_variant")
+    _checked(dsts, nelem, dcode, "device", "ar_reduce_variant")
     v = VARIANTS[variant] if isinstance(variant, str) else variant
     _check(lib().ar_reduce_variant(_ptrs(srcs), _ptrs(dsts), len(dsts), nelem, dcode, _dtype_code(wire_dtype),
                                    v, grid_blocks, _stream(stream)), "ar_reduce_variant")
@@ -210,6 +249,8 @@ def ar_reduce_host(h_srcs, h_dsts, d_srcs=None, d_dsts=None, nelem=None, dst_dty
     staging buffers, or (``d_srcs``/``d_dsts`` None) with the kernel reading
     and writing the pinned host buffers directly; ordered on ``stream``."""
     nelem, dcode = _infer(d_srcs if d_srcs is not None else h_srcs, nelem, dst_dtype)
+    for xs, where in ((h_srcs, "host"), (h_dsts, "host"), (d_srcs, "device"), (d_dsts, "device")):
+        _checked(xs, nelem, dcode, where, "ar_reduce_host")
     _check(lib().ar_reduce_host(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode, _dtype_code(wire_dtype),
                                 _ptrs(d_srcs), _ptrs(d_dsts), _stream(stream)), "ar_reduce_host")
 
@@ -256,6 +297,9 @@ def ar_wire_pack(src, wire, nelem=None, dst_dtype=None, wire_dtype="bf16", strea
         nelem = src.numel()
     if dst_dtype is None:
         dst_dtype = src.dtype
+    dcode, wcode = _dtype_code(dst_dtype), _dtype_code(wire_dtype)
+    _checked([src], nelem, dcode, "device", "ar_wire_pack")
+    _checked([wire], nelem, wcode, "device", "ar_wire_pack")
     _check(lib().ar_wire_pack(_ptr(src), _ptr(wire), nelem, _dtype_code(dst_dtype), _dtype_code(wire_dtype),
                               _stream(stream)), "ar_wire_pack")
 
@@ -269,5 +313,7 @@ def ar_reduce_host_noalloc(h_srcs, h_dsts, nelem=None, dst_dtype=None, wire_dtyp
     At most AR_NOALLOC_SCRATCH_BYTES of staging per call; calls that overlap
     on the GPU share that area and must not run at the same time."""
     nelem, dcode = _infer(h_srcs, nelem, dst_dtype)
+    _checked(h_srcs, nelem, dcode, "host", "ar_reduce_host_noalloc")
+    _checked(h_dsts, nelem, dcode, "host", "ar_reduce_host_noalloc")
     _check(lib().ar_reduce_host_noalloc(_ptrs(h_srcs), _ptrs(h_dsts), len(h_dsts), nelem, dcode,
                                         _dtype_code(wire_dtype), _stream(stream)), "ar_reduce_host_noalloc")

@@ -192,17 +192,19 @@ def test_zero_elements_is_a_no_op(ctx):
 def test_errors_write_nothing(ctx):
     tps.ar_init(2, 1000)
     ctx.R = None  # the next test re-initialises with its own limits
-    a = torch.randn(1000, device="cuda")
-    b = torch.randn(1000, device="cuda")
-    out = torch.full((1000,), 7.0, device="cuda")
+    a = torch.randn(1001, device="cuda")  # one element more than max_elems
+    b = torch.randn(1001, device="cuda")
+    out = torch.full((1001,), 7.0, device="cuda")
     with pytest.raises(tps.ARError) as e:
         tps.ar_reduce([a, b], [out], nelem=1001, dst_dtype="f32")
     assert e.value.status == 3
+    with pytest.raises(ValueError):  # the binding: a destination shorter than the call
+        tps.ar_reduce([a, b], [out[:500]], nelem=1000, dst_dtype="f32")
     with pytest.raises(tps.ARError) as e:
         tps.ar_reduce([a, b], [a[10:]], nelem=990, dst_dtype="f32")
     assert e.value.status == 5
     with pytest.raises(tps.ARError) as e:
-        tps.ar_reduce([a], [out], dst_dtype="f32")  # one source short of R=2
+        tps.ar_reduce([a], [out], nelem=1000, dst_dtype="f32")  # one source short of R=2
     assert e.value.status == 1
     torch.cuda.synchronize()
     assert (out == 7.0).all()
