@@ -148,6 +148,17 @@ def _checked(xs, nelem, dcode, where, call):
     return xs
 
 
+def _reach(x) -> int | None:
+    """Bytes a kernel may touch from a CUDA tensor's first element to the end
+    of its storage (None for raw addresses); a non-CUDA tensor is refused."""
+    if x is None or isinstance(x, int) or not hasattr(x, "data_ptr"):
+        return None
+    if x.device.type != "cuda":
+        raise TypeError(f"a {x.device.type} tensor where a device buffer is needed")
+    st = x.untyped_storage()
+    return st.data_ptr() + st.nbytes() - x.data_ptr()
+
+
 def _dtype_code(d) -> int:
     if isinstance(d, int):
         return d
@@ -268,6 +279,7 @@ def make_layout(ne0, ne1, src_row_bytes=None, dst_row_bytes=None, residual=None,
     if dst_row_bytes is not None:
         L.dst_row_bytes = (ctypes.c_int64 * len(dst_row_bytes))(*dst_row_bytes)
     L.residual = _ptr(residual)
+    L._residual_obj = residual  # kept for the binding's reach check
     if residual is not None and residual_row_bytes is None:
         residual_row_bytes = ne0 * residual.element_size()
     L.residual_row_bytes = residual_row_bytes or 0
@@ -280,7 +292,25 @@ def make_layout(ne0, ne1, src_row_bytes=None, dst_row_bytes=None, residual=None,
 
 def ar_reduce_ex(srcs, dsts, layout: ArLayout, dst_dtype, wire_dtype="bf16", stream=None) -> None:
     """Reduction over an ar_layout (row strides, inactive ranks as None
-    sources, residual or bias)."""
+    sources, residual or bias).  The rows of each CUDA tensor must lie inside
+    its storage."""
+    es = ESIZE[_dtype_code(dst_dtype)]
+    ne0, ne1 = layout.ne0, layout.ne1
+    if ne0 * ne1:
+        def need(stride):
+            return (ne1 - 1) * stride + ne0 * es
+        for kind, xs, rows in (("source", srcs, layout.src_row_bytes), ("destination", dsts, layout.dst_row_bytes)):
+            for k, x in enumerate(xs):
+                reach = _reach(x)
+                n = need(rows[k] if rows else ne0 * es)
+                if reach is not None and reach < n:
+                    raise ValueError(f"ar_reduce_ex: {kind} {k} reaches {reach} bytes, its rows span {n}")
+        res = getattr(layout, "_residual_obj", None)
+        reach = _reach(res)
+        if reach is not None:
+            n = ne0 * es if layout.residual_row_bytes == 0 else need(layout.residual_row_bytes)
+            if reach < n:
+                raise ValueError(f"ar_reduce_ex: the residual reaches {reach} bytes, its rows span {n}")
     _check(lib().ar_reduce_ex(_ptrs(srcs), _ptrs(dsts), len(dsts), ctypes.byref(layout), _dtype_code(dst_dtype),
                               _dtype_code(wire_dtype), _stream(stream)), "ar_reduce_ex")
 

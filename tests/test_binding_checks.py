@@ -48,3 +48,19 @@ def test_the_wire_buffer_is_sized_in_wire_elements():
         ar._checked([np.zeros(63, np.uint16)], 64, ar.AR_BF16, "host", "t")
     ar._checked([src], 64, ar.AR_F32, "host", "t")
     ar._checked([12345, None], 64, ar.AR_F32, "device", "t")  # raw addresses pass unchecked
+
+
+def test_reach_needs_a_cuda_tensor():
+    """Raw addresses are not checked; host tensors are refused (the reach of
+    CUDA views is tested on the GPU)."""
+    from tensor_partial_sum_gb300 import ar
+    assert ar._reach(None) is None and ar._reach(1234) is None
+    with pytest.raises(TypeError):
+        ar._reach(torch.zeros(8))
+
+
+def test_ex_refuses_rows_past_the_storage_on_cpu_tensors():
+    a = torch.zeros(64)
+    lay = tps.make_layout(8, 8)
+    with pytest.raises(TypeError):
+        tps.ar_reduce_ex([a, a], [a.clone()], lay, "f32")

@@ -318,3 +318,21 @@ def test_wire_pack_offsets(dst, wire, offs, n):
                for h in range(16 // ES[dst]))
     if fits:
         assert tps.ar_query("last_variant") == tps.ar.VARIANTS["bandwidth"]
+
+
+def test_binding_refuses_rows_past_the_storage():
+    """Rows of a strided view may use the storage past the view's own last
+    element (padding), but not past the storage's end."""
+    ne0, ne1, pad = 100, 4, 28
+    tps.ar_init(2, ne0 * ne1)
+    back = torch.zeros(ne1 * (ne0 + pad), device="cuda")
+    rows = back.view(ne1, ne0 + pad)[:, :ne0]  # not contiguous; reaches the storage's end
+    stride = [(ne0 + pad) * 4] * 2
+    out = torch.zeros(ne0 * ne1, device="cuda")
+    tps.ar_reduce_ex([rows, rows], [out], tps.make_layout(ne0, ne1, src_row_bytes=stride), "f32")
+    torch.cuda.synchronize()
+    tail = back[(ne0 + pad):]  # one row less of storage
+    with pytest.raises(ValueError, match="source 0 reaches"):
+        tps.ar_reduce_ex([tail, rows], [out], tps.make_layout(ne0, ne1, src_row_bytes=stride), "f32")
+    with pytest.raises(ValueError, match="destination 0 reaches"):
+        tps.ar_reduce_ex([rows, rows], [out[1:]], tps.make_layout(ne0, ne1), "f32")
