@@ -283,7 +283,7 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             // thread; a grid that covers the tensor unless a persistent grid
             // is asked for
             const bool wide = k.wide_bytes == 32 && off32 >= 0;
-            const tps::VecKernels &vk = wide ? k.wide : k.v16;
+            const tps::VecKernels &vk = wide ? k.wide : k.bw16;
             const int vec_bytes = wide ? k.wide_bytes : 16;
             fn = (c.R <= 2 ? vk.few : vk.many)[nc];
             threads = kBandwidthThreads;

@@ -27,8 +27,9 @@ struct Kernels {
     ExKernelFn ex32[2][2];   // [R >= 3][residual], 32-byte vectors (f32 only, else nullptr)
     PackKernelFn pack[2];    // [16-byte vectors]
     PackKernelFn pack32;     // 32-byte source vectors (f32 only, else nullptr)
-    VecKernels v16;    // 16-byte vectors
-    VecKernels wide;   // the bandwidth width: 32-byte vectors for f32, 16 for 16-bit types
+    VecKernels v16;    // 16-byte vectors, unrolled loops: the latency launch
+    VecKernels bw16;   // 16-byte vectors, rolled loops: the bandwidth launch
+    VecKernels wide;   // the bandwidth launch's widest: 32-byte vectors for f32, bw16 otherwise
     int wide_bytes;    // 32 or 16
     KernelFn scalar[2];  // [NC]
     KernelFn naive;
@@ -40,22 +41,25 @@ const Kernels &kernels_f32(int wire);
 const Kernels &kernels_f16(int wire);
 const Kernels &kernels_bf16(int wire);
 
-template <int Td, int Tw, int VB>
+// UNR: rank and destination loops unrolled (the latency launch).
+template <int Td, int Tw, int VB, bool UNR>
 VecKernels make_vec_kernels() {
-    return VecKernels{{ar_reduce_kernel<Td, Tw, VB, 1, 2, false>, ar_reduce_kernel<Td, Tw, VB, 1, 2, true>},
-                      {ar_reduce_kernel<Td, Tw, VB, 1, 4, false>, ar_reduce_kernel<Td, Tw, VB, 1, 4, true>}};
+    return VecKernels{
+        {ar_reduce_kernel<Td, Tw, VB, 1, 2, false, UNR>, ar_reduce_kernel<Td, Tw, VB, 1, 2, true, UNR>},
+        {ar_reduce_kernel<Td, Tw, VB, 1, 4, false, UNR>, ar_reduce_kernel<Td, Tw, VB, 1, 4, true, UNR>}};
 }
 
 // Kernel set of one (dst, wire) pair.
 template <int Td, int Tw>
 Kernels make_kernels() {
     Kernels k{};
-    k.v16 = make_vec_kernels<Td, Tw, 16>();
+    k.v16 = make_vec_kernels<Td, Tw, 16, true>();
+    k.bw16 = make_vec_kernels<Td, Tw, 16, false>();
     if constexpr (Td == kF32) {
-        k.wide = make_vec_kernels<Td, Tw, 32>();
+        k.wide = make_vec_kernels<Td, Tw, 32, false>();
         k.wide_bytes = 32;
     } else {
-        k.wide = k.v16;
+        k.wide = k.bw16;
         k.wide_bytes = 16;
     }
     k.ex[0][0][0] = ar_reduce_ex_kernel<Td, Tw, 2, false, false>;
