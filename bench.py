@@ -57,7 +57,11 @@ def dist_init(world: int, backend: str):
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
-        dist.barrier()
+        if dist.get_backend() == "nccl":  # on this rank's own GPU, named so NCCL need not guess it
+            import torch
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
 
 
 def max_over_ranks(x: float, device=None) -> float:
