@@ -134,6 +134,20 @@ def test_common_offset_many_ranks_in_place(ctx, variant):
     assert tps.ar_query("last_variant") == tps.ar.VARIANTS[variant]
 
 
+@pytest.mark.parametrize("grid", [1, 3, 152])
+def test_common_offset_with_a_persistent_grid(ctx, grid):
+    """The head is done by CTA 0 after its share of the rounds, whatever the
+    grid; with a tail too, the last CTA does both jobs' elements."""
+    n = 300_007
+    srcs = srcs_for(300 + grid, 2, n, "bf16")
+    exp = expect(srcs, "bf16", "f16")
+    outs, backs = run(ctx, srcs, 2, "bf16", "f16", variant="bandwidth", grid=grid, src_offsets=[3, 3],
+                      dst_offsets=[3, 3], pad=64)
+    for o in outs:
+        assert_same(o, exp, "bf16", f"offset 3, grid {grid}")
+    check_guards(backs)
+
+
 def test_tma_refuses_an_offset(ctx):
     """The bulk-copy variant needs 16-byte starts even when the offset is shared."""
     srcs = srcs_for(78, 2, 4096, "f32")
