@@ -61,6 +61,7 @@ struct Context {
     int tma_tile = 16384;            // AR_TMA_TILE: largest tile, bytes (1024 .. 32768, 1 KiB multiples)
     int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
     int64_t tma_drop_tile = -1;      // test hook (AR_Q_TMA_DROP_TILE), -1 = off
+    int pdl = 1;                     // AR_PDL: vector kernels launch as programmatic dependents
 };
 
 void destroy_pipe(HostPipe &p) {
@@ -329,8 +330,23 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         p.rounds = (nv + per_round - 1) / per_round;
         p.chunk = p.rounds ? (nv + p.rounds * grid - 1) / (p.rounds * grid) : 0;
     }
-    fn<<<grid, threads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    // The vector kernel waits (griddepcontrol.wait) for the kernel before it
+    // on the stream before touching memory, so it may be launched as a
+    // programmatic dependent: its launch then overlaps that kernel's last
+    // wave.  The element-wise kernels have no such wait and launch plainly.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (plan_vec_bytes > 0 && c.pdl) ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
     c.last_variant = variant;
     return AR_OK;
 }
@@ -462,7 +478,7 @@ int ar_init(int R, size_t max_elems) {
     };
     if (!env_int("AR_TMA_STAGES", 2, tps::kTmaMaxStages, &c.tma_stages) ||
         !env_int("AR_TMA_TILE", 1024, 32768, &c.tma_tile) || c.tma_tile % 1024 ||
-        !env_int("AR_TMA_CTAS_PER_SM", 1, 4, &c.tma_ctas_per_sm))
+        !env_int("AR_TMA_CTAS_PER_SM", 1, 4, &c.tma_ctas_per_sm) || !env_int("AR_PDL", 0, 1, &c.pdl))
         return AR_ERR_INVALID_ARG;
     if (const char *s = getenv("AR_LATENCY_MAX_BYTES")) {
         char *end = nullptr;

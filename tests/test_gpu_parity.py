@@ -593,3 +593,53 @@ def test_tma_bounded_wait_runs_out_reports_and_context_survives(ctx):
     torch.cuda.synchronize()
     assert tps.ar_query("device_status") == 0
     assert_same(to_host(out, "f32"), expect(srcs, "f32", "bf16"), "f32", "after a timed-out launch")
+
+
+def test_dependent_launch_still_honours_event_waits(ctx):
+    """The vector kernels launch as programmatic dependents of the kernel
+    before them on the stream.  A cross-stream event wait between the two
+    must still hold: the second reduction reads partials that another
+    stream writes only after a delay."""
+    n = 1 << 20
+    ctx.ensure(2, n)
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    a = torch.zeros(n, device="cuda")
+    b = torch.zeros(n, device="cuda")
+    warm = torch.ones(n, device="cuda")
+    out1 = torch.empty(n, device="cuda")
+    out2 = torch.empty(n, device="cuda")
+    torch.cuda.synchronize()
+    ready = torch.cuda.Event()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(20_000_000)  # a bounded delay (about 10 ms) before the partials are written
+        a.fill_(1.5)
+        b.fill_(2.25)
+        ready.record(side)
+    tps.ar_reduce([warm, warm], [out1], wire_dtype="f32", stream=main)  # the kernel before, on `main`
+    main.wait_event(ready)
+    tps.ar_reduce([a, b], [out2], wire_dtype="f32", stream=main)
+    torch.cuda.synchronize()
+    assert tps.ar_query("last_variant") == tps.ar.VARIANTS["latency"]
+    assert (out1 == 2.0).all()
+    assert (out2 == 3.75).all()
+
+
+def test_dependent_launch_after_a_copy_on_the_same_stream(ctx):
+    """Kernel, then a host-to-device copy, then a reduction of the copied
+    partials, all on one stream: the reduction sees the copy."""
+    n = 1 << 22
+    ctx.ensure(2, n)
+    main = torch.cuda.Stream()
+    warm = torch.ones(n, device="cuda")
+    a = torch.zeros(n, device="cuda")
+    host = torch.full((n,), 4.0).pin_memory()
+    out1 = torch.empty(n, device="cuda")
+    out2 = torch.empty(n, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(main):
+        tps.ar_reduce([warm, warm], [out1], wire_dtype="f32", stream=main)
+        a.copy_(host, non_blocking=True)
+        tps.ar_reduce([a, warm], [out2], wire_dtype="f32", stream=main)
+    torch.cuda.synchronize()
+    assert (out1 == 2.0).all()
+    assert (out2 == 5.0).all()
