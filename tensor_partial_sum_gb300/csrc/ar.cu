@@ -194,6 +194,24 @@ int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t 
 }
 
 // Launch one reduction; the caller holds g_mu and has validated the arguments.
+// Launch a kernel that runs griddepcontrol.launch_dependents and
+// griddepcontrol.wait before touching memory: as a programmatic dependent of
+// the kernel before it on the stream when `pdl`, else plainly.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, unsigned threads, cudaStream_t stream, bool pdl,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
                   int wire_dtype, int variant, int grid_blocks, cudaStream_t stream, bool explicit_variant) {
     Context &c = g_ctx;
@@ -334,16 +352,8 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     // on the stream before touching memory, so it may be launched as a
     // programmatic dependent: its launch then overlaps that kernel's last
     // wave.  The element-wise kernels have no such wait and launch plainly.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (plan_vec_bytes > 0 && c.pdl) ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), static_cast<unsigned>(threads), stream,
+                         plan_vec_bytes > 0 && c.pdl, p) != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
     }
@@ -818,8 +828,11 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     }
     if (gx < 1) gx = 1;
     const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
-    fn<<<dim3(static_cast<unsigned>(gx), gy), threads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(gx), gy), static_cast<unsigned>(threads), stream, c.pdl != 0,
+                         p) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
     c.last_variant = vec ? AR_VARIANT_BANDWIDTH : AR_VARIANT_SCALAR;
     return AR_OK;
 }
@@ -869,8 +882,11 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     if (grid < 1) grid = 1;
     const void *s0 = static_cast<const char *>(src) + head * es;
     void *w0 = static_cast<char *>(wire) + head * ew;
-    fn<<<static_cast<unsigned>(grid), 256, 0, stream>>>(s0, w0, nelem, static_cast<int>(head));
-    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), 256u, stream, g_ctx.pdl != 0, s0, w0,
+                         static_cast<unsigned long long>(nelem), static_cast<int>(head)) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
     g_ctx.last_variant = vec ? AR_VARIANT_BANDWIDTH : AR_VARIANT_SCALAR;
     return AR_OK;
 }

@@ -64,6 +64,8 @@ template <int Td, int Tw, int RB, bool RES, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant__ ArExParams p) {
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
+    pdl_launch_dependents();
+    pdl_wait();  // the kernel before this one on the stream has finished
     for (size_t row = blockIdx.y; row < p.ne1; row += gridDim.y) {
         if constexpr (VEC) {
             // elements of the row before its first VB-byte boundary
@@ -154,6 +156,8 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
             static_cast<unsigned short *>(wire)[i] = static_cast<unsigned short>(narrow2<Tw>(a, b) & 0xFFFFu);
         }
     };
+    pdl_launch_dependents();
+    pdl_wait();  // the kernel before this one on the stream has finished
     if constexpr (VEC) {
         const size_t nvec = nelem / V;
         const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
