@@ -61,7 +61,7 @@ struct Context {
     int tma_tile = 16384;            // AR_TMA_TILE: largest tile, bytes (1024 .. 32768, 1 KiB multiples)
     int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
     int64_t tma_drop_tile = -1;      // test hook (AR_Q_TMA_DROP_TILE), -1 = off
-    int pdl = 1;                     // AR_PDL: vector kernels launch as programmatic dependents
+    int pdl = 1;                     // AR_PDL: kernels launch as programmatic dependents
 };
 
 void destroy_pipe(HostPipe &p) {
@@ -153,6 +153,25 @@ const char *variant_name(int v) {
     }
 }
 
+// Launch a kernel that runs griddepcontrol.launch_dependents and
+// griddepcontrol.wait before touching memory: as a programmatic dependent of
+// the kernel before it on the stream when `pdl`, else plainly.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, unsigned threads, size_t smem, cudaStream_t stream,
+                             bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 int grid_cap(long long want, long long cap) {
     if (want < 1) want = 1;
     if (want > cap) want = cap;
@@ -187,31 +206,16 @@ int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t 
     long long grid = grid_blocks > 0 ? grid_blocks : static_cast<long long>(c.sm_count) * c.tma_ctas_per_sm;
     if (grid > static_cast<long long>(plan.ntiles)) grid = static_cast<long long>(plan.ntiles);
     if (grid < 1) grid = 1;
-    k.tma<<<static_cast<unsigned>(grid), tps::kTmaThreads, smem, stream>>>(p, plan);
-    if (cudaGetLastError() != cudaSuccess) return AR_ERR_CUDA;
+    if (launch_dependent(k.tma, dim3(static_cast<unsigned>(grid)), tps::kTmaThreads, smem, stream, c.pdl != 0, p,
+                         plan) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
     c.last_variant = AR_VARIANT_TMA;
     return AR_OK;
 }
 
 // Launch one reduction; the caller holds g_mu and has validated the arguments.
-// Launch a kernel that runs griddepcontrol.launch_dependents and
-// griddepcontrol.wait before touching memory: as a programmatic dependent of
-// the kernel before it on the stream when `pdl`, else plainly.
-template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, unsigned threads, cudaStream_t stream, bool pdl,
-                             Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(threads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fn, args...);
-}
-
 int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
                   int wire_dtype, int variant, int grid_blocks, cudaStream_t stream, bool explicit_variant) {
     Context &c = g_ctx;
@@ -348,12 +352,12 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         p.rounds = (nv + per_round - 1) / per_round;
         p.chunk = p.rounds ? (nv + p.rounds * grid - 1) / (p.rounds * grid) : 0;
     }
-    // The vector kernel waits (griddepcontrol.wait) for the kernel before it
-    // on the stream before touching memory, so it may be launched as a
-    // programmatic dependent: its launch then overlaps that kernel's last
-    // wave.  The element-wise kernels have no such wait and launch plainly.
-    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), static_cast<unsigned>(threads), stream,
-                         plan_vec_bytes > 0 && c.pdl, p) != cudaSuccess) {
+    // The kernels wait (griddepcontrol.wait) for the kernel before them on
+    // the stream before touching memory, so they may be launched as
+    // programmatic dependents: the launch then overlaps that kernel's last
+    // wave.  The naive cross-check kernel has no such wait and launches plainly.
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), static_cast<unsigned>(threads), 0, stream,
+                         c.pdl != 0 && variant != AR_VARIANT_NAIVE, p) != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
     }
@@ -828,7 +832,7 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     }
     if (gx < 1) gx = 1;
     const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
-    if (launch_dependent(fn, dim3(static_cast<unsigned>(gx), gy), static_cast<unsigned>(threads), stream, c.pdl != 0,
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(gx), gy), static_cast<unsigned>(threads), 0, stream, c.pdl != 0,
                          p) != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
@@ -882,7 +886,7 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     if (grid < 1) grid = 1;
     const void *s0 = static_cast<const char *>(src) + head * es;
     void *w0 = static_cast<char *>(wire) + head * ew;
-    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), 256u, stream, g_ctx.pdl != 0, s0, w0,
+    if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), 256u, 0, stream, g_ctx.pdl != 0, s0, w0,
                          static_cast<unsigned long long>(nelem), static_cast<int>(head)) != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;

@@ -395,6 +395,8 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
 template <int Td, int Tw, bool NC>
 __global__ void __launch_bounds__(256) ar_scalar_kernel(const __grid_constant__ ArParams p) {
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+    pdl_launch_dependents();
+    pdl_wait();
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.nelem; i += step)
         reduce_elem<Td, Tw, NC>(p, i);
 }

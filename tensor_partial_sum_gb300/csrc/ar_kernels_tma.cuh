@@ -98,6 +98,8 @@ template <int Td, int Tw>
 __global__ void __launch_bounds__(kTmaThreads) ar_tma_kernel(const __grid_constant__ ArParams p,
                                                                 const __grid_constant__ TmaPlan plan) {
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_launch_dependents();
+    pdl_wait();  // the kernel before this one on the stream has finished
     unsigned long long *full = reinterpret_cast<unsigned long long *>(smem);
     unsigned long long *empty = full + kTmaMaxStages;
     volatile unsigned *abort_flag = reinterpret_cast<volatile unsigned *>(empty + kTmaMaxStages);
