@@ -643,3 +643,21 @@ def test_dependent_launch_after_a_copy_on_the_same_stream(ctx):
     torch.cuda.synchronize()
     assert (out1 == 2.0).all()
     assert (out2 == 5.0).all()
+
+
+@pytest.mark.parametrize("pdl", ["0", "1"])
+def test_plain_and_dependent_launches_give_the_same_bits(ctx, pdl, monkeypatch):
+    """AR_PDL=0 launches every kernel plainly; the bits do not change."""
+    monkeypatch.setenv("AR_PDL", pdl)
+    tps.ar_init(3, 1 << 20)
+    ctx.R = None  # the next test re-initialises with its own limits (and without the variable)
+    n = 300_007
+    srcs = srcs_for(4242, 3, n, "f32")
+    exp = expect(srcs, "f32", "bf16")
+    for v in VARIANTS:
+        d_srcs = [to_device(s, "f32") for s in srcs]
+        d_dsts = [torch.empty(n, device="cuda") for _ in range(2)]
+        tps.ar_reduce_variant(d_srcs, d_dsts, v, dst_dtype="f32", wire_dtype="bf16")
+        torch.cuda.synchronize()
+        for d in d_dsts:
+            assert_same(to_host(d, "f32"), exp, "f32", f"AR_PDL={pdl} variant={v}")
