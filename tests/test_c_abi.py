@@ -38,3 +38,18 @@ def test_c_program_reduces_on_the_gpu(tmp_path):
                    ldflags=["-L", os.path.join(CUDA, "lib64"), "-lcudart", f"-Wl,-rpath,{os.path.join(CUDA, 'lib64')}"])
     out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.startswith("ok"), out.stdout + out.stderr
+
+
+@pytest.mark.gpu
+def test_host_cost_of_a_decode_call(tmp_path):
+    """Validating, choosing and enqueuing a decode-sized call from C costs
+    a few microseconds at most (the figures are printed for the record)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    exe = _compile("host_cost.c", str(tmp_path / "host_cost"), cflags=["-I", os.path.join(CUDA, "include")],
+                   ldflags=["-L", os.path.join(CUDA, "lib64"), "-lcudart", f"-Wl,-rpath,{os.path.join(CUDA, 'lib64')}"])
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.startswith("ok"), out.stdout + out.stderr
+    fields = dict(kv.split("=") for kv in out.stdout.split()[1:])
+    print(out.stdout.strip())
+    assert float(fields["eager_us"]) < 20 and float(fields["capture_us"]) < 20
