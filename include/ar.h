@@ -94,7 +94,7 @@ typedef enum {
                                  CTAs; all loads of two or four ranks issued together */
     AR_VARIANT_SCALAR = 4,    /* element-wise path used when the buffers' offsets differ */
     AR_VARIANT_TMA = 5        /* shared-memory staging: a producer warp bulk-copies (cp.async.bulk)
-                                 R source tiles per stage, eight warps fold them, one thread
+                                 R source tiles per stage, sixteen warps fold them, one thread
                                  bulk-stores the result tile to every destination; one CTA per SM.
                                  Needs 16-byte aligned buffers.  Never chosen by AUTO (an
                                  AR_VARIANT environment override with offset buffers takes
