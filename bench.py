@@ -531,12 +531,26 @@ def bench_decode(dev, stream):
         b.record(stream)
     torch.cuda.synchronize(dev)
     eager = a.elapsed_time(b) * 1e3 / w.calls
+    # the same calls through prepared calls (buffer checks and pointer arrays done once)
+    prepared = [tps.PreparedReduce(s, d, nelem=w.nelem, dst_dtype="f32", wire_dtype=w.wire, stream=stream)
+                for s, d in calls]
+    with torch.cuda.stream(stream):
+        for k in range(min(100, w.calls)):
+            prepared[k]()
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for k in range(w.calls):
+            prepared[k]()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_prepared = a.elapsed_time(b) * 1e3 / w.calls
     variant = {v: k for k, v in tps.ar.VARIANTS.items()}[tps.ar_query("last_variant")]
     del graph, buf
     return {"us_per_call": round(statistics.median(times), 3), "unit": "µs/call",
             "target_us": 5.0, "workload": f"{w.name}: {w.describe()}", "variant": variant,
             "timing": f"one CUDA graph of {w.calls} ar_reduce nodes, median of 5 replays",
             "us_per_call_eager_stream": round(eager, 3),
+            "us_per_call_eager_prepared": round(eager_prepared, 3),
             "bytes_per_call": w.bytes_per_call}
 
 

@@ -9,5 +9,5 @@ from .ar import (  # noqa: F401
     AR_BF16, AR_F16, AR_F32, ARError, DTYPE_CODES, ar_check_args, ar_free, ar_init,
     ar_query, ar_reduce, ar_reduce_host, ar_reduce_variant, ar_set_option,
     ar_status_string, library_path, ArLayout, make_layout, ar_reduce_ex, ar_check_layout, ar_wire_pack,
-    ar_reduce_host_noalloc, AR_NOALLOC_SCRATCH_BYTES,
+    ar_reduce_host_noalloc, AR_NOALLOC_SCRATCH_BYTES, PreparedReduce,
 )

@@ -236,6 +236,32 @@ def ar_reduce_variant(srcs, dsts, variant="auto", grid_blocks=0, nelem=None, dst
                                    v, grid_blocks, _stream(stream)), "ar_reduce_variant")
 
 
+class PreparedReduce:
+    """One ar_reduce_variant call with its arguments fixed: the buffer
+    checks and the pointer arrays are done once, so each call is a single
+    C call (for eager code that repeats the same reduction, e.g. every
+    decode step; a CUDA graph removes the per-call cost altogether).  Holds
+    references to the buffers it was given."""
+
+    def __init__(self, srcs, dsts, nelem=None, dst_dtype=None, wire_dtype="bf16", variant="auto", stream=None):
+        nelem, dcode = _infer(srcs, nelem, dst_dtype)
+        _checked(srcs, nelem, dcode, "device", "PreparedReduce")
+        _checked(dsts, nelem, dcode, "device", "PreparedReduce")
+        self._keep = (list(srcs), list(dsts))
+        self._args = (_ptrs(srcs), _ptrs(dsts), len(dsts), nelem, dcode, _dtype_code(wire_dtype),
+                      VARIANTS[variant] if isinstance(variant, str) else variant, 0)
+        self._stream = None if stream is None else _stream(stream)
+        self._fn = lib().ar_reduce_variant
+
+    def __call__(self, stream=None):
+        """Enqueue the reduction on ``stream`` (default: the one given at
+        preparation, else torch's current stream)."""
+        s = _stream(stream) if stream is not None else (self._stream if self._stream is not None else _stream(None))
+        st = self._fn(*self._args, s)
+        if st != AR_OK:
+            raise ARError(st, "ar_reduce")
+
+
 def ar_check_args(R, srcs, dsts, n_dsts, nelem, max_elems, dst_dtype, wire_dtype) -> int:
     """Host-only validation; returns the status code (does not raise)."""
     return lib().ar_check_args(R, _ptrs(srcs), _ptrs(dsts), n_dsts, nelem, max_elems,

@@ -64,3 +64,9 @@ def test_ex_refuses_rows_past_the_storage_on_cpu_tensors():
     lay = tps.make_layout(8, 8)
     with pytest.raises(TypeError):
         tps.ar_reduce_ex([a, a], [a.clone()], lay, "f32")
+
+
+def test_prepared_call_checks_its_buffers_once():
+    a = torch.zeros(64)
+    with pytest.raises(TypeError, match="cpu tensor"):
+        tps.PreparedReduce([a, a], [a.clone()])

@@ -661,3 +661,21 @@ def test_plain_and_dependent_launches_give_the_same_bits(ctx, pdl, monkeypatch):
         torch.cuda.synchronize()
         for d in d_dsts:
             assert_same(to_host(d, "f32"), exp, "f32", f"AR_PDL={pdl} variant={v}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "latency", "bandwidth", "scalar"])
+def test_prepared_call_gives_the_same_bits(ctx, variant):
+    n = 50_003
+    ctx.ensure(3, n)
+    srcs = srcs_for(909, 3, n, "bf16")
+    exp = expect(srcs, "bf16", "f16")
+    d_srcs = [to_device(s, "bf16") for s in srcs]
+    d_dsts = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    call = tps.PreparedReduce(d_srcs, d_dsts, wire_dtype="f16", variant=variant)
+    for _ in range(3):  # repeatable
+        for d in d_dsts:
+            d.fill_(7)
+        call()
+        torch.cuda.synchronize()
+        for d in d_dsts:
+            assert_same(to_host(d, "bf16"), exp, "bf16", f"prepared {variant}")
