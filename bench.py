@@ -600,6 +600,10 @@ def main(argv=None):
         p.error("--warmup must be at least 3")
     if args.steps < 1:
         p.error("--steps must be at least 1")
+    world = dist_env()[2]
+    if args.gpus != world:
+        p.error(f"--gpus {args.gpus} but {world} process(es): for N > 1 launch one process per GPU "
+                f"(python -m torch.distributed.run --nproc-per-node N ... bench.py --gpus N)")
     if args.impl == "reference":
         run_reference(args)
     else:
