@@ -238,24 +238,35 @@ def oracle_rate(srcs, w, seconds: float, steps: int = 0, threads: int = 1):
     sized to take about seconds / steps each.  Returns (GB/s, elapsed,
     sample text)."""
     from concurrent.futures import ThreadPoolExecutor
-    probe_rows = max(1, min(w.ne1, (1 << 16) // w.ne0))
-    t = time.perf_counter()
-    oracle_step(w, srcs, 0, probe_rows)
-    per_row = max((time.perf_counter() - t) / probe_rows, 1e-9) / threads
-    budget = seconds / steps if steps else seconds
-    rows = int(min(w.ne1, max(1, budget / per_row)))
-    reps = steps if steps else max(1, int(seconds / (per_row * rows)))
-    threads = max(1, min(threads, rows))
-    cuts = [rows * k // threads for k in range(threads + 1)]
+
+    def one_pass(pool, rows, nt):
+        cuts = [rows * k // nt for k in range(nt + 1)]
+        list(pool.map(lambda k: oracle_step(w, srcs, cuts[k], cuts[k + 1]), range(nt)))
+
     with ThreadPoolExecutor(threads) as pool:
+        # a pass costs about a + b * rows: fit a and b on two probe passes
+        r1 = max(1, min(w.ne1, threads))
+        r2 = max(r1 + 1, min(w.ne1, max(8 * threads, (1 << 18) // w.ne0)))
+        cost = []
+        for r in (r1, r2):
+            t = time.perf_counter()
+            one_pass(pool, r, min(threads, r))
+            cost.append(time.perf_counter() - t)
+        b = max((cost[1] - cost[0]) / (r2 - r1), 1e-9)
+        a = max(cost[0] - b * r1, 0.0)
+        budget = seconds / steps if steps else seconds
+        rows = int(min(w.ne1, max(1, (budget - a) / b)))
+        per_pass = a + b * rows
+        reps = steps if steps else max(1, int(seconds / per_pass))
+        nt = max(1, min(threads, rows))
         t = time.perf_counter()
         for _ in range(reps):
-            list(pool.map(lambda k: oracle_step(w, srcs, cuts[k], cuts[k + 1]), range(threads)))
+            one_pass(pool, rows, nt)
         el = time.perf_counter() - t
     moved = w.bytes_per_call * rows / w.ne1 * reps
     return (moved / el / 1e9, el,
             f"first {rows} of {w.ne1} rows ({rows * w.ne0} of {w.nelem} elements) of the workload, "
-            f"{reps} pass(es) on {threads} thread(s), {el:.1f} s")
+            f"{reps} pass(es) on {nt} thread(s), {el:.1f} s")
 
 
 # ---- our arm -----------------------------------------------------------------
