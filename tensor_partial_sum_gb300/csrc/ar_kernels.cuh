@@ -389,16 +389,49 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
     }
 }
 
-// Element-wise grid-stride kernel: the path for pointers that are not all
-// 16-byte aligned.  Same arithmetic as ar_reduce_kernel, one element per
-// thread per iteration.
+// Element-wise grid-stride kernel: the path for buffers at different
+// offsets from a vector boundary.  Same arithmetic as ar_reduce_kernel.  Each
+// thread takes E elements a grid stride apart per iteration (every warp
+// access stays coalesced) and loads them for four ranks at a time before
+// folding, so 4*E loads are in flight per thread instead of R.
 template <int Td, int Tw, bool NC>
 __global__ void __launch_bounds__(256) ar_scalar_kernel(const __grid_constant__ ArParams p) {
+    constexpr int E = 4;
+    constexpr int RB = 4;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     pdl_launch_dependents();
     pdl_wait();
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.nelem; i += step)
-        reduce_elem<Td, Tw, NC>(p, i);
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + (E - 1) * step < p.nelem; i += E * step) {
+        float acc[E];
+#pragma unroll
+        for (int r0 = 0; r0 < kMaxRanks; r0 += RB) {  // constant parameter offsets (see reduce_span)
+            if (r0 >= p.R) break;
+            float v[RB][E];
+#pragma unroll
+            for (int j = 0; j < RB; ++j)
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    v[j][e] = r0 + j < p.R ? load_elem<Td, NC>(p.src[r0 + j], static_cast<long long>(i + e * step))
+                                           : 0.0f;
+#pragma unroll
+            for (int j = 0; j < RB; ++j)
+                if (r0 + j < p.R) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float w = wire1<Td, Tw>(v[j][e]);
+                        acc[e] = (r0 + j == 0) ? w : __fadd_rn(acc[e], w);
+                    }
+                }
+        }
+#pragma unroll
+        for (int d = 0; d < kMaxDsts; ++d) {
+            if (d >= p.n_dsts) break;
+#pragma unroll
+            for (int e = 0; e < E; ++e) store_elem<Td>(p.dst[d], static_cast<long long>(i + e * step), acc[e]);
+        }
+    }
+    for (; i < p.nelem; i += step) reduce_elem<Td, Tw, NC>(p, static_cast<long long>(i));
 }
 
 // Naive cross-check kernel in the style of ggml_cuda_ar_add_kernel: one
