@@ -827,7 +827,8 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
         }
         gx = (need + threads - 1) / threads;
     } else {
-        gx = (static_cast<long long>(L->ne0) + threads - 1) / threads;
+        // four elements per thread (the element-wise path's batch)
+        gx = (static_cast<long long>(L->ne0) + 4ll * threads - 1) / (4ll * threads);
         if (gx > 1024) gx = 1024;
     }
     if (gx < 1) gx = 1;

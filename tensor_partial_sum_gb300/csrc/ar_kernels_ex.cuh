@@ -128,9 +128,39 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
             const size_t u = v - vpr;
             if (v >= vpr && u < h + t) ex_reduce_elem<Td, Tw, RES>(p, row, u < h ? u : u + vpr * V);
         } else {
-            for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.ne0;
-                 i += static_cast<size_t>(gridDim.x) * blockDim.x)
-                ex_reduce_elem<Td, Tw, RES>(p, row, i);
+            // E elements a grid stride apart per thread, their loads for four
+            // ranks at a time in flight before the fold
+            constexpr int E = 4;
+            const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+            size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+            for (; i + (E - 1) * stride < p.ne0; i += E * stride) {
+                float acc[E];
+                for (int r0 = 0; r0 < p.R; r0 += 4) {
+                    float v[4][E];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < E; ++e)
+                            v[j][e] = r0 + j < p.R ? ex_operand<Td, Tw>(p, r0 + j, row, i + e * stride) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (r0 + j < p.R) {
+#pragma unroll
+                            for (int e = 0; e < E; ++e) acc[e] = (r0 + j == 0) ? v[j][e] : __fadd_rn(acc[e], v[j][e]);
+                        }
+                }
+                if constexpr (RES) {
+                    const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], load_elem<Td, false>(rb, i + e * stride));
+                }
+                for (int d = 0; d < p.n_dsts; ++d) {
+                    char *db = static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) store_elem<Td>(db, static_cast<long long>(i + e * stride), acc[e]);
+                }
+            }
+            for (; i < p.ne0; i += stride) ex_reduce_elem<Td, Tw, RES>(p, row, i);
         }
     }
 }
