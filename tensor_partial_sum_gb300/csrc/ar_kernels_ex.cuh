@@ -170,15 +170,15 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
 // each thread converts one VB-byte vector of sources (16 or 32 bytes); the
 // last CTA does the tail element by element, and CTA 0 the `head` elements
 // at indices -head .. -1 (the host shifts both pointers forward past them
-// when the buffers start off a vector boundary).
+// when the buffers start off a vector boundary).  Otherwise element-wise,
+// four elements in flight per thread.
 template <int Td, int Tw, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem,
                                                       int head) {
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
     constexpr int WB = V * Elem<Tw>::bytes;  // output bytes per vector: 8, 16 or 32
-    auto one = [&](long long i) {
-        float a = load_elem<Td, false>(src, i);
+    auto put = [&](long long i, float a) {
         if constexpr (Tw == kF32) {
             static_cast<float *>(wire)[i] = a;
         } else {
@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
             static_cast<unsigned short *>(wire)[i] = static_cast<unsigned short>(narrow2<Tw>(a, b) & 0xFFFFu);
         }
     };
+    auto one = [&](long long i) { put(i, load_elem<Td, false>(src, i)); };
     pdl_launch_dependents();
     pdl_wait();  // the kernel before this one on the stream has finished
     if constexpr (VEC) {
@@ -223,9 +224,18 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
             if (k < head) one(-1 - k);
         }
     } else {
-        for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nelem;
-             i += static_cast<size_t>(gridDim.x) * blockDim.x)
-            one(static_cast<long long>(i));
+        // four elements a grid stride apart per thread: loads first, then stores
+        constexpr int E = 4;
+        const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+        size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        for (; i + (E - 1) * stride < nelem; i += E * stride) {
+            float a[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) a[e] = load_elem<Td, false>(src, static_cast<long long>(i + e * stride));
+#pragma unroll
+            for (int e = 0; e < E; ++e) put(static_cast<long long>(i + e * stride), a[e]);
+        }
+        for (; i < nelem; i += stride) one(static_cast<long long>(i));
     }
 }
 
