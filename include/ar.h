@@ -111,10 +111,11 @@ typedef enum {
  * scalar|tma), AR_LATENCY_MAX_BYTES (size switch, bytes of sources plus
  * destinations), AR_TMA_STAGES (2..8, default 3), AR_TMA_TILE (largest
  * tile in bytes, a multiple of 1024 up to 32768, default 16384),
- * AR_TMA_CTAS_PER_SM (1..4, default 1), AR_PDL (1 = default: every kernel but
- * NAIVE's launches as a programmatic dependent of the kernel before it on the
- * stream, which it waits for before touching memory; 0 = plain launches),
- * AR_LOG=1 (one line per init to stderr).
+ * AR_TMA_CTAS_PER_SM (1..4, default 1), AR_PDL (1 = default: on a created
+ * stream, every kernel but NAIVE's launches as a programmatic dependent of
+ * the kernel before it on the stream, which it waits for before touching
+ * memory; launches on the default streams stay plain; 0 = plain launches
+ * everywhere), AR_LOG=1 (one line per init to stderr).
  * Calling it again replaces the context.  Returns AR_OK, AR_ERR_INVALID_ARG,
  * AR_ERR_UNSUPPORTED (the device is not sm_103) or AR_ERR_CUDA (no device).
  */

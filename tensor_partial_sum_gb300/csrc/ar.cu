@@ -168,7 +168,10 @@ cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, unsigned threads,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    // Not on the default streams: their implicit ordering against other
+    // streams is left exactly as a plain launch has it.
+    const bool default_stream = stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread;
+    cfg.numAttrs = (pdl && !default_stream) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 

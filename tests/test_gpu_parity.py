@@ -654,10 +654,13 @@ def test_plain_and_dependent_launches_give_the_same_bits(ctx, pdl, monkeypatch):
     n = 300_007
     srcs = srcs_for(4242, 3, n, "f32")
     exp = expect(srcs, "f32", "bf16")
+    stream = torch.cuda.Stream()  # a created stream: the default streams always launch plainly
     for v in VARIANTS:
         d_srcs = [to_device(s, "f32") for s in srcs]
         d_dsts = [torch.empty(n, device="cuda") for _ in range(2)]
-        tps.ar_reduce_variant(d_srcs, d_dsts, v, dst_dtype="f32", wire_dtype="bf16")
+        torch.cuda.synchronize()
+        tps.ar_reduce_variant(d_srcs, d_dsts, v, dst_dtype="f32", wire_dtype="bf16", stream=stream)
+        tps.ar_reduce_variant(d_srcs, d_dsts, v, dst_dtype="f32", wire_dtype="bf16", stream=stream)
         torch.cuda.synchronize()
         for d in d_dsts:
             assert_same(to_host(d, "f32"), exp, "f32", f"AR_PDL={pdl} variant={v}")
