@@ -336,3 +336,12 @@ def test_binding_refuses_rows_past_the_storage():
         tps.ar_reduce_ex([tail, rows], [out], tps.make_layout(ne0, ne1, src_row_bytes=stride), "f32")
     with pytest.raises(ValueError, match="destination 0 reaches"):
         tps.ar_reduce_ex([rows, rows], [out[1:]], tps.make_layout(ne0, ne1), "f32")
+
+
+@pytest.mark.parametrize("ne0,pad", [(8, 0), (13, 3)])
+def test_more_rows_than_the_grid_holds(ne0, pad):
+    """ne1 above 65 535 (the grid's y limit): CTAs stride over the rows; both
+    the vector path (ne0 = 8, packed) and the element-wise one (ne0 = 13 with
+    differing strides) cover every row."""
+    run_ex(2, ne0, 70_001, "f32", "bf16", seed=ne0, src_pad=[pad, 2 * pad], dst_pad=(0,), residual=True,
+           res_pad=0)
