@@ -256,6 +256,9 @@ def oracle_rate(srcs, w, seconds: float, steps: int = 0, threads: int = 1):
         a = max(cost[0] - b * r1, 0.0)
         budget = seconds / steps if steps else seconds
         rows = int(min(w.ne1, max(1, (budget - a) / b)))
+        # at least one row per thread, so that every core works in every pass
+        # (a pass then costs a + b * threads, which may exceed a tiny budget)
+        rows = max(rows, min(threads, w.ne1))
         per_pass = a + b * rows
         reps = steps if steps else max(1, int(seconds / per_pass))
         nt = max(1, min(threads, rows))
