@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
 // last CTA does the tail element by element, and CTA 0 the `head` elements
 // at indices -head .. -1 (the host shifts both pointers forward past them
 // when the buffers start off a vector boundary).  Otherwise element-wise,
-// four elements in flight per thread.
+// eight elements in flight per thread.
 template <int Td, int Tw, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem,
                                                       int head) {
@@ -224,8 +224,9 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
             if (k < head) one(-1 - k);
         }
     } else {
-        // four elements a grid stride apart per thread: loads first, then stores
-        constexpr int E = 4;
+        // eight elements a grid stride apart per thread: loads first, then
+        // stores (8 measured 7% faster than 4 here; the reductions keep 4)
+        constexpr int E = 8;
         const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
         size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         for (; i + (E - 1) * stride < nelem; i += E * stride) {
