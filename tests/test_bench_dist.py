@@ -71,3 +71,28 @@ def test_reference_arm_two_ranks_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["unit"] == "GB/s" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_line_has_every_contract_key():
+    """One process: the reference arm's JSON line carries the keys the
+    benchmark contract lists, with the types it expects."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3", "--warmup", "3",
+           "--ref-seconds", "1", "--workload", "tp_small"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    rec = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1])
+    for k, t in [("metric", str), ("value", float), ("unit", str), ("n_gpus", int), ("steps", int), ("warmup", int),
+                 ("ms_per_step", float), ("higher_is_better", bool), ("scaling", str), ("dtype", str),
+                 ("data", str), ("config", dict), ("cpu_baseline", dict), ("e2e", dict)]:
+        assert isinstance(rec[k], t), (k, rec.get(k))
+    assert rec["vs_baseline"] is None and rec["n_gpus"] == 1 and rec["steps"] == 3
+    assert rec["config"]["workload"].startswith("tp_small")
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"] and cb["sample"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_gpus_flag_must_match_the_process_count():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert out.returncode != 0 and "launch one process per GPU" in out.stderr
