@@ -209,3 +209,13 @@ def test_check_layout_residual_and_overlap():
     assert chk_l(dsts=[0x40000000, 0x40000000 + 64]) == OVERLAP
     # an inactive rank's pointer is never read, so it cannot overlap
     assert chk_l(srcs=[0x1000000, 0x40000000 + 8], inactive=(1,)) == OK
+
+
+def test_every_environment_knob_is_documented():
+    """Each environment variable the library reads is described in the header."""
+    src = open(os.path.join(os.path.dirname(HEADER), "..", "tensor_partial_sum_gb300", "csrc", "ar.cu")).read()
+    names = set(re.findall(r'(?:getenv|env_int)\("([A-Z_]+)"', src))
+    assert {"AR_VARIANT", "AR_PDL"} <= names
+    header = open(HEADER).read()
+    missing = [n for n in sorted(names) if n not in header]
+    assert not missing, missing
