@@ -36,11 +36,14 @@
  *   - Device pointers are CUDA addresses the device that was current at
  *     ar_init can access: device memory, or pinned/managed host memory
  *     (which the kernel then reads or writes over the CPU-GPU link); host
- *     pointers are ordinary (ideally pinned) host memory.  The caller owns every buffer and the stream; the library
- *     keeps no pointer after a call returns and allocates nothing per call.
+ *     pointers are ordinary (ideally pinned) host memory.  The caller owns
+ *     every buffer and the stream; the library keeps no pointer after a call
+ *     returns and allocates nothing per call.
  *   - Calls that take a stream only enqueue work on it and return; results
- *     are ready when the stream reaches that point.  No call synchronizes,
- *     so ar_reduce and ar_reduce_variant can be captured in a CUDA graph.
+ *     are ready when the stream reaches that point.  No call synchronizes
+ *     (a host call given pageable memory waits for CUDA's synchronous
+ *     pageable copies, see ar_reduce_host_noalloc), so ar_reduce and
+ *     ar_reduce_variant can be captured in a CUDA graph.
  *   - On any status other than AR_OK nothing has been enqueued or written,
  *     except AR_ERR_CUDA from a launch, after which the stream's state is
  *     whatever CUDA reports.
@@ -222,10 +225,13 @@ int ar_set_option(int key, int64_t value);
  *                   be memory the GPU can reach (cudaHostAlloc /
  *                   cudaHostRegister pinned memory, or managed memory);
  *                   otherwise AR_ERR_INVALID_ARG.
- * Everything else as for ar_reduce.  Either way the work starts after what
- * is already enqueued on `stream`, and `stream` reaches the end of this
- * call only when the host results are complete.  Results are identical to
- * one ar_reduce over device copies of the same tensors.
+ * Everything else as for ar_reduce, and the host buffers obey ar_reduce's
+ * buffer rules too: element-aligned, and a host destination may be exactly
+ * a host source but may not partly overlap any host source or other host
+ * destination (AR_ERR_OVERLAP, nothing enqueued).  Either way the work
+ * starts after what is already enqueued on `stream`, and `stream` reaches
+ * the end of this call only when the host results are complete.  Results
+ * are identical to one ar_reduce over device copies of the same tensors.
  */
 int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem,
                    int dst_dtype, int wire_dtype, void *const *d_srcs, void *const *d_dsts,
@@ -319,9 +325,13 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
  * the library, reduces there, and copies every destination back to its host
  * buffer, all enqueued on `stream` (results are valid once `stream` reaches
  * the end of this call).  It allocates nothing: no cudaMalloc, no cudaFree,
- * no allocating library routine.  Same arguments and results as
- * ar_reduce_host with NULL staging arrays, except that the host buffers may
- * be ordinary pageable memory.
+ * no allocating library routine.  Same arguments, buffer rules (partial
+ * overlap of host buffers is AR_ERR_OVERLAP) and results as ar_reduce_host
+ * with NULL staging arrays, except that the host buffers may be ordinary
+ * pageable memory.  CUDA copies pageable memory synchronously, so with
+ * pageable buffers the call itself waits until `stream` has reached its
+ * copies; it holds no library lock while it waits, so other threads' calls
+ * go on.
  *
  * Limits and rules:
  *   - The staging area is AR_NOALLOC_SCRATCH_BYTES (64 MiB) of device
@@ -329,9 +339,14 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
  *     exits.  A call needs R + n_dsts buffers of nelem elements, each rounded
  *     up to 256 bytes; a call that needs more returns AR_ERR_TOO_LARGE and
  *     does nothing.
- *   - The first call on a device looks up the staging area's device address
- *     (once per device, with that device current); make that first call
- *     before any stream capture.
+ *   - The first call on a device after each ar_init looks up the staging
+ *     area's device address (once, with that device current); make that
+ *     first call before any stream capture.  ar_init and ar_free forget the
+ *     address, so a context created after cudaDeviceReset finds the area
+ *     where the new device context holds it.  If another thread runs
+ *     ar_init or ar_free while a call is under way, the call may return
+ *     AR_ERR_NOT_INITIALIZED after its copies into the staging area were
+ *     enqueued (the caller's buffers are then not written).
  *   - Every call on a GPU uses the same staging area, and each call leaves
  *     its data there: nothing in it has to start at zero, because every call
  *     writes its inputs before reading them.  Calls whose work overlaps on

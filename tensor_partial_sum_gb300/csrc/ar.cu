@@ -91,6 +91,14 @@ bool create_pipe(HostPipe &p) {
 
 std::mutex g_mu;
 Context g_ctx;
+// Incremented (under g_mu) by every ar_init and ar_free: a call that drops
+// the lock half way through can tell whether the context was replaced.
+unsigned long long g_ctx_gen = 0;
+
+// Forget the cached device addresses of the no-allocation staging area (a
+// new context may follow a device reset, after which the area can sit at a
+// new address).  Called with g_mu held.
+void forget_noalloc_addresses();
 
 size_t elem_bytes(int dtype) {
     switch (dtype) {
@@ -468,6 +476,8 @@ int ar_init(int R, size_t max_elems) {
     destroy_pipe(g_ctx.pipe);
     if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
     g_ctx = Context{};
+    ++g_ctx_gen;
+    forget_noalloc_addresses();
     int dev = -1, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return AR_ERR_CUDA;
@@ -523,6 +533,8 @@ void ar_free(void) {
     destroy_pipe(g_ctx.pipe);
     if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
     g_ctx = Context{};
+    ++g_ctx_gen;
+    forget_noalloc_addresses();
 }
 
 int ar_reduce_variant(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
@@ -614,13 +626,14 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
     if (!d_srcs) return reduce_host_direct_locked(h_srcs, h_dsts, n_dsts, nelem, dst_dtype, wire_dtype, stream);
     const void *srcs_c[AR_MAX_RANKS];
     for (int r = 0; r < c.R; ++r) srcs_c[r] = d_srcs[r];
-    const int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+    int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
     if (st != AR_OK) return st;
     if (nelem == 0) return AR_OK;
-    for (int r = 0; r < c.R; ++r)
-        if (!h_srcs[r]) return AR_ERR_INVALID_ARG;
-    for (int d = 0; d < n_dsts; ++d)
-        if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
+    // The host buffers obey the same rules.  A host destination that partly
+    // overlaps a host source would be written (copy back of chunk k) before
+    // a later chunk's copy in has read the source bytes it shares.
+    st = ar_check_args(c.R, h_srcs, h_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+    if (st != AR_OK) return st;
     {  // the launch below checks the device too, but only after copies would be queued
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
@@ -899,6 +912,8 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     return AR_OK;
 }
 
+}  // extern "C"
+
 // ---- staging without allocation ---------------------------------------------
 //
 // ar_reduce_host_noalloc stages host partials through this fixed array
@@ -911,59 +926,81 @@ namespace {
 static_assert(AR_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[AR_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch per device ordinal, looked up once per
-// device (guarded by g_mu).  In host code the array's name is only a host-side
-// handle, never an address a kernel may use.
+// Device address of g_noalloc_scratch per device ordinal, looked up by the
+// first call on that device after each ar_init (guarded by g_mu).  In host
+// code the array's name is only a host-side handle, never an address a kernel
+// may use.
 constexpr int kMaxScratchDevices = 64;
 void *g_noalloc_addr[kMaxScratchDevices] = {};
 
+void forget_noalloc_addresses() {
+    for (void *&a : g_noalloc_addr) a = nullptr;
+}
+
 }  // namespace
+
+extern "C" {
 
 int ar_reduce_host_noalloc(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem, int dst_dtype,
                            int wire_dtype, cudaStream_t stream) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
-    const Context &c = g_ctx;
-    if (!h_srcs || !h_dsts || n_dsts < 1 || n_dsts > AR_MAX_DSTS) return AR_ERR_INVALID_ARG;
-    const size_t es = elem_bytes(dst_dtype);
-    if (!es || !elem_bytes(wire_dtype)) return AR_ERR_UNSUPPORTED;
-    if (nelem > c.max_elems) return AR_ERR_TOO_LARGE;
-    if (nelem == 0) return AR_OK;
-    for (int r = 0; r < c.R; ++r)
-        if (!h_srcs[r]) return AR_ERR_INVALID_ARG;
-    for (int d = 0; d < n_dsts; ++d)
-        if (!h_dsts[d]) return AR_ERR_INVALID_ARG;
-    // every staged buffer starts on a 256-byte boundary of the array
-    const size_t bytes = nelem * es;
-    const size_t slot = (bytes + 255) / 256 * 256;
-    if (slot < bytes || static_cast<size_t>(c.R + n_dsts) > AR_NOALLOC_SCRATCH_BYTES / slot)
-        return AR_ERR_TOO_LARGE;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
-    if (dev != c.device || dev < 0 || dev >= kMaxScratchDevices) return AR_ERR_INVALID_ARG;
-    if (!g_noalloc_addr[dev]) {
-        // first call on this device (which is current here): find the array's device address
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return AR_ERR_CUDA;
+    // Under the lock: check the call and find the staging area.  The copies
+    // are enqueued without the lock, because a copy from or to pageable host
+    // memory can block the calling thread until the stream gets there, and
+    // other library calls must not wait behind it.
+    int R = 0;
+    unsigned long long gen = 0;
+    size_t bytes = 0, slot = 0;
+    char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+        const Context &c = g_ctx;
+        if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
+        // the rules of ar_reduce, applied to the host buffers: counts, types,
+        // NULL pointers, element alignment, partial overlap
+        const int st = ar_check_args(c.R, h_srcs, h_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+        if (st != AR_OK || nelem == 0) return st;
+        // every staged buffer starts on a 256-byte boundary of the array
+        bytes = nelem * elem_bytes(dst_dtype);
+        slot = (bytes + 255) / 256 * 256;
+        if (slot < bytes || static_cast<size_t>(c.R + n_dsts) > AR_NOALLOC_SCRATCH_BYTES / slot)
+            return AR_ERR_TOO_LARGE;
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+        if (dev != c.device || dev < 0 || dev >= kMaxScratchDevices) return AR_ERR_INVALID_ARG;
+        if (!g_noalloc_addr[dev]) {
+            // first call on this device since ar_init (the device is current here)
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+                cudaGetLastError();
+                return AR_ERR_CUDA;
+            }
+            g_noalloc_addr[dev] = ptr;
         }
-        g_noalloc_addr[dev] = ptr;
+        if (c.fault_inject) return AR_ERR_CUDA;
+        base = static_cast<char *>(g_noalloc_addr[dev]);
+        R = c.R;
+        gen = g_ctx_gen;
     }
-    if (c.fault_inject) return AR_ERR_CUDA;
-    char *base = static_cast<char *>(g_noalloc_addr[dev]);
     const void *d_srcs[AR_MAX_RANKS];
     void *d_dsts[AR_MAX_DSTS];
-    for (int r = 0; r < c.R; ++r) {
+    for (int r = 0; r < R; ++r) {
         d_srcs[r] = base + static_cast<size_t>(r) * slot;
         if (cudaMemcpyAsync(const_cast<void *>(d_srcs[r]), h_srcs[r], bytes, cudaMemcpyHostToDevice, stream) !=
             cudaSuccess)
             return AR_ERR_CUDA;
     }
-    for (int d = 0; d < n_dsts; ++d) d_dsts[d] = base + static_cast<size_t>(c.R + d) * slot;
-    const int st = launch_locked(d_srcs, d_dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, stream,
-                                 false);
-    if (st != AR_OK) return st;
+    for (int d = 0; d < n_dsts; ++d) d_dsts[d] = base + static_cast<size_t>(R + d) * slot;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        // ar_init or ar_free on another thread since the checks: the staging
+        // area may have moved, so stop before the launch (only the staging
+        // area has been written)
+        if (!g_ctx.ready || g_ctx_gen != gen) return AR_ERR_NOT_INITIALIZED;
+        const int st = launch_locked(d_srcs, d_dsts, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0,
+                                     stream, false);
+        if (st != AR_OK) return st;
+    }
     for (int d = 0; d < n_dsts; ++d)
         if (cudaMemcpyAsync(h_dsts[d], d_dsts[d], bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
             return AR_ERR_CUDA;

@@ -73,6 +73,11 @@ def mismatches(a, b, name: str) -> np.ndarray:
 
 
 def assert_same(a, b, name: str, what: str = ""):
+    ab, bb = as_bits(a), as_bits(b)
+    if ab.shape != bb.shape:
+        raise AssertionError(f"{what}: {ab.size} elements against {bb.size}")
+    if np.array_equal(ab, bb):  # the common case, without the NaN masks' temporaries
+        return
     bad = mismatches(a, b, name)
     if bad.size:
         i = int(bad[0])

@@ -121,6 +121,21 @@ def test_check_args_overlap():
     assert chk(srcs=[0x10000, 0x10000 + 128], nelem=n) == OK
 
 
+def test_check_args_overlap_on_host_arrays():
+    """The same rule guards the host buffers of ar_reduce_host and
+    ar_reduce_host_noalloc (they run it on the host pointers): views of one
+    numpy buffer that partly overlap are refused, an exact alias is not."""
+    import numpy as np
+    n = 1000
+    back = np.zeros(3 * n, dtype=np.float32)
+    srcs = [back[:n], back[2 * n:]]
+    assert chk(srcs=srcs, dsts=[back[n // 2:n // 2 + n]], nelem=n) == OVERLAP
+    assert chk(srcs=srcs, dsts=[back[n:2 * n]], nelem=n) == OK
+    assert chk(srcs=srcs, dsts=[srcs[1]], nelem=n) == OK
+    other = np.zeros(2 * n, dtype=np.float32)
+    assert chk(srcs=srcs, dsts=[other[:n], other[n - 1:2 * n - 1]], nelem=n) == OVERLAP
+
+
 def test_calls_before_init():
     tps.ar_free()
     tps.ar_free()  # a second free is harmless

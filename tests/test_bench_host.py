@@ -1,5 +1,7 @@
 """bench.py's host-side helpers without a GPU: the clock summary, the
-throttle rule, and reading traffic from the committed ncu summary."""
+throttle rule, reading traffic from the committed ncu counters, the
+roofline record and the step counts of the workloads measured beside the
+headline."""
 import datetime as dt
 import os
 import sys
@@ -34,15 +36,46 @@ def test_short_region_falls_back_to_all_samples_and_throttle_rule():
     assert bench.ClockSampler.summarize([], t, t)["samples"] == 0
 
 
-def test_traffic_field_follows_the_kernel_sources():
-    v = bench.traffic_per_launch("prefill")
-    text = open(bench.TRAFFIC_SUMMARY).read()
-    recorded = [l for l in text.splitlines() if l.startswith("- source_digest:")][0]
-    if bench.sources_digest() in recorded:
-        assert isinstance(v, int) and v > 100_000_000
-    else:
-        assert v is None  # the kernel changed since the counters were taken
+def test_traffic_field_follows_the_kernel_sources(tmp_path):
+    import json
+    recorded = json.load(open(bench.TRAFFIC_FILE))["workloads"]
+    assert "prefill" in recorded
+    for name, e in recorded.items():
+        v = bench.traffic_per_launch(name)
+        if e["source_digest"] == bench.sources_digest():
+            assert v == e["dram_bytes_per_launch"] and v > 0.9 * e["algorithmic_bytes_per_launch"]
+        else:
+            assert v is None  # the kernel changed since the counters were taken
     assert bench.traffic_per_launch("decode") is None
+    # a stale digest, a missing file and a malformed file all read as "no figure"
+    p = tmp_path / "t.json"
+    p.write_text(json.dumps({"workloads": {"prefill": {"source_digest": "0", "dram_bytes_per_launch": 5}}}))
+    assert bench.traffic_per_launch("prefill", str(p)) is None
+    p.write_text(json.dumps({"workloads": {"prefill": {"source_digest": bench.sources_digest(),
+                                                       "dram_bytes_per_launch": 5}}}))
+    assert bench.traffic_per_launch("prefill", str(p)) == 5
+    assert bench.traffic_per_launch("prefill", str(tmp_path / "none.json")) is None
+    p.write_text("not json")
+    assert bench.traffic_per_launch("prefill", str(p)) is None
+
+
+def test_config_steps_are_whole_graph_replays_of_enough_time():
+    from tensor_partial_sum_gb300 import workloads as W
+    small, big = W.WORKLOADS["tp_small"], W.WORKLOADS["f16_edges"]
+    k = bench.config_steps(small, 20, 64)
+    assert k % 64 == 0 and k * (small.bytes_per_call / 6.8e12 + 1e-6) > 1.9e-3  # about 2 ms of launches
+    assert bench.config_steps(big, 20, 20) == 20
+    assert bench.config_steps(big, 25, 20) == 40
+
+
+def test_roofline_record_has_measured_and_nominal_fractions():
+    from tensor_partial_sum_gb300 import workloads as W
+    w = W.WORKLOADS["prefill"]
+    r = bench.roofline(w, 20e-6)
+    assert r["achieved"] == round(w.bytes_per_call / 20e-6 / 1e9, 1)
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert abs(r["frac_nominal"] - r["achieved"] / 8000.0) < 1e-3 and r["nominal_peak"] == 8000.0
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel_us"] == 20.0
 
 
 def test_aggregate():

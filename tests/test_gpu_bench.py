@@ -16,7 +16,7 @@ def test_bench_line_has_the_contract_keys():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "300", "--warmup", "5", "--e2e-steps", "3",
-           "--cpu-seconds", "1", "--sustain", "0.2"]
+           "--cpu-seconds", "1", "--cpu-seconds-per-config", "0.5", "--sustain", "0.2"]
     out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-3000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
@@ -40,4 +40,20 @@ def test_bench_line_has_the_contract_keys():
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
-    assert d["decode"]["us_per_call"] > 0
+    assert d["dtype"] == "f32" and r["frac_nominal"] > 0 and r["nominal_peak"] == 8000.0
+    # one record per workload the benchmark is specified on
+    cfgs = d["configs"]
+    assert [cfgs[n]["cfg"] for n in ("tp_small", "decode", "prefill", "bf16_t3", "f16_edges")] == [1, 2, 3, 4, 5]
+    assert cfgs["prefill"]["roofline"] == r and cfgs["prefill"]["value"] == d["value"]
+    for name, rec in cfgs.items():
+        assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1, name
+        assert rec["cpu_baseline"]["value"] > 0, name
+        if name == "decode":
+            assert 0 < rec["us_per_call"] < 5.0 and rec["cpu_baseline"]["unit"] == "µs/call"
+            continue
+        rr = rec["roofline"]
+        assert abs(rr["frac"] - rr["achieved"] / rr["peak"]) < 1e-3 and rr["frac_nominal"] > 0, name
+        assert abs(rr["achieved"] - rec["value"]) / rec["value"] < 1e-2, name
+        assert rec["us_per_call"] > 0 and {"sm_mhz", "reasons"} <= set(rec["clocks"]), name
+        if rec["class"] == "prefill":
+            assert rr["frac"] > 0.8, (name, rr["frac"])  # the bar the benchmark is specified with

@@ -2,10 +2,10 @@
 benchmark uses: automatic variant choice, a CUDA graph on a created stream,
 launches back to back as programmatic dependents.
 
-The oracle is element-wise, so it is evaluated on a gathered sample of
-indices (the first and last 64 Ki elements, where the planted edge values
-and the tail sit, plus 1 Mi random ones); properties that hold at any size
-(every destination identical) are checked on the whole tensor."""
+Every element of every destination is compared with the oracle, bit for bit
+(any NaN matches any NaN).  The oracle runs over contiguous ranges on every
+host core (tests/whole.py), which takes about a second for the largest
+workload."""
 import numpy as np
 import pytest
 import torch
@@ -13,6 +13,7 @@ import torch
 import oracle
 import tensor_partial_sum_gb300 as tps
 from tensor_partial_sum_gb300 import workloads as W
+from tests import whole
 from tests.gpu_util import TORCH_DTYPE, to_device, to_host
 from tests.libcasts import assert_same
 
@@ -51,13 +52,6 @@ def as_benchmarked(call, outs):
     del g
 
 
-def sample_indices(n, seed=0):
-    rng = np.random.Generator(np.random.PCG64(seed))
-    k = min(n, 1 << 16)
-    idx = np.concatenate([np.arange(k), np.arange(n - k, n), rng.integers(0, n, min(n, 1 << 20))])
-    return np.unique(idx)
-
-
 @pytest.mark.parametrize("name", ["tp_small", "prefill", "bf16_t3", "f16_edges"])
 def test_full_size_workload(name):
     w = W.WORKLOADS[name]
@@ -68,13 +62,9 @@ def test_full_size_workload(name):
     as_benchmarked(lambda s: tps.ar_reduce(src_t, dst_t, nelem=w.nelem, dst_dtype=w.dst, wire_dtype=w.wire,
                                            stream=s), dst_t)
     del src_t
-    ref = dst_t[0].view(torch.int16 if w.elem_bytes == 2 else torch.int32)
-    for d in dst_t[1:]:
-        assert torch.equal(d.view(ref.dtype), ref), "destinations differ"
-    idx = sample_indices(w.nelem, seed=w.seed)
-    exp = oracle.reduce([s[idx] for s in srcs], 1, w.dst, w.wire)[0]
-    got = to_host(dst_t[0], w.dst)[idx]
-    assert_same(got, exp, w.dst, f"{name} sampled")
+    exp = whole.reduce(srcs, w.dst, w.wire)
+    for d, t in enumerate(dst_t):
+        assert_same(to_host(t, w.dst), exp, w.dst, f"{name} destination {d}, all {w.nelem} elements")
 
 
 def test_decode_every_call_graph_captured():
@@ -112,8 +102,8 @@ def test_decode_every_call_graph_captured():
                                   "prefill_pack"])
 def test_full_size_extended_workload(name):
     """The extended entry points at the prefill size, set up as the benchmark
-    sets them up; the oracle checks a sample of whole rows (the first and last
-    16 and 64 random ones)."""
+    sets them up; every row of every destination is compared with the
+    oracle, and the row padding must stay untouched."""
     w = W.WORKLOADS[name]
     srcs = W.generate(w)
     ne0, ne1, pad, es = w.ne0, w.ne1, w.row_pad, w.elem_bytes
@@ -126,15 +116,11 @@ def test_full_size_extended_workload(name):
             t[:, :ne0].copy_(to_device(a, w.dst).view(ne1, ne0))
         return t
 
-    rng = np.random.Generator(np.random.PCG64(w.seed))
-    rows = np.unique(np.concatenate([np.arange(16), np.arange(ne1 - 16, ne1), rng.integers(0, ne1, 64)]))
-    idx = (rows[:, None] * ne0 + np.arange(ne0)[None, :]).ravel()
     if w.op == "pack":
         src = to_device(srcs[0], w.dst)
         out = torch.empty(w.nelem, dtype=TORCH_DTYPE[w.wire], device="cuda")
         as_benchmarked(lambda s: tps.ar_wire_pack(src, out, dst_dtype=w.dst, wire_dtype=w.wire, stream=s), [out])
-        exp = oracle.wire_pack(srcs[0][idx], w.dst, w.wire)
-        assert_same(to_host(out, w.wire)[idx], exp, w.wire, name)
+        assert_same(to_host(out, w.wire), whole.wire_pack(srcs[0], w.dst, w.wire), w.wire, name)
         return
     s_t = [None if r in w.inactive else rows_tensor(srcs[r]) for r in range(w.R)]
     d_t = [rows_tensor() for _ in range(w.n_dsts)]
@@ -144,16 +130,10 @@ def test_full_size_extended_workload(name):
                              residual_row_bytes=0 if w.residual == "row" else None, inactive=w.inactive)
     as_benchmarked(lambda s: tps.ar_reduce_ex(s_t, d_t, layout, w.dst, w.wire, stream=s),
                    [d[:, :ne0] for d in d_t])
-    res, res_stride = None, None
-    if w.residual == "full":
-        res = srcs[w.R][idx]
-    elif w.residual == "row":
-        res, res_stride = srcs[w.R], 0
-    holes = [None if r in w.inactive else srcs[r][idx] for r in range(w.R)]
-    exp = oracle.reduce_2d(holes, 1, w.dst, w.wire, ne0, rows.size, inactive=w.inactive, residual=res,
-                           residual_stride=res_stride)[0]
-    for d in d_t:
-        got = to_host(d[:, :ne0].contiguous(), w.dst).reshape(ne1, ne0)[rows].ravel()
-        assert_same(got, exp, w.dst, name)
+    exp = whole.reduce_rows(srcs[:w.R], w.dst, w.wire, ne0, ne1, inactive=w.inactive,
+                            residual=srcs[w.R] if w.residual else None, residual_kind=w.residual)
+    for k, d in enumerate(d_t):
+        got = to_host(d[:, :ne0].contiguous(), w.dst)
+        assert_same(got, exp, w.dst, f"{name} destination {k}, all rows")
         if pad:
             assert (d[:, ne0:] == 0).all(), "row padding written"
