@@ -39,11 +39,14 @@ def test_short_region_falls_back_to_all_samples_and_throttle_rule():
 def test_traffic_field_follows_the_kernel_sources(tmp_path):
     import json
     recorded = json.load(open(bench.TRAFFIC_FILE))["workloads"]
-    assert "prefill" in recorded
+    assert {"tp_small", "prefill", "bf16_t3", "f16_edges"} <= set(recorded)
     for name, e in recorded.items():
         v = bench.traffic_per_launch(name)
+        # no launch moves more than its algorithmic bytes (nothing read twice); writes may
+        # trail them while destinations are still dirty in L2
+        assert e["dram_bytes_per_launch"] <= 1.01 * e["algorithmic_bytes_per_launch"], name
         if e["source_digest"] == bench.sources_digest():
-            assert v == e["dram_bytes_per_launch"] and v > 0.9 * e["algorithmic_bytes_per_launch"]
+            assert v == e["dram_bytes_per_launch"]
         else:
             assert v is None  # the kernel changed since the counters were taken
     assert bench.traffic_per_launch("decode") is None
