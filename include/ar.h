@@ -118,7 +118,10 @@ typedef enum {
  * stream, every kernel but NAIVE's launches as a programmatic dependent of
  * the kernel before it on the stream, which it waits for before touching
  * memory; launches on the default streams stay plain; 0 = plain launches
- * everywhere), AR_LOG=1 (one line per init to stderr).
+ * everywhere), AR_L2_PREFETCH (1 = default: the first wave of CTAs of the
+ * LATENCY and BANDWIDTH kernels asks L2 for its source vectors before that
+ * wait, so they load while the kernel ahead drains; 0 = off; results are the
+ * same either way), AR_LOG=1 (one line per init to stderr).
  * Calling it again replaces the context.  Returns AR_OK, AR_ERR_INVALID_ARG,
  * AR_ERR_UNSUPPORTED (the device is not sm_103) or AR_ERR_CUDA (no device).
  */

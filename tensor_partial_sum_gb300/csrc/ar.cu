@@ -62,6 +62,7 @@ struct Context {
     int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
     int64_t tma_drop_tile = -1;      // test hook (AR_Q_TMA_DROP_TILE), -1 = off
     int pdl = 1;                     // AR_PDL: kernels launch as programmatic dependents
+    int l2_prefetch = 1;             // AR_L2_PREFETCH: the first wave prefetches its sources before the wait
 };
 
 void destroy_pipe(HostPipe &p) {
@@ -120,24 +121,75 @@ const Kernels &kernels_for(int dst, int wire) {
     return tps::kernels_bf16(wire);
 }
 
-// Resident CTAs per SM of a kernel (queried once per kernel, then cached).
+// Resident CTAs per SM of a kernel at a block size (queried once, then
+// cached in an open-addressed table keyed by the kernel's address and the
+// block size; guarded by g_mu).
 struct OccEntry {
-    KernelFn fn;
+    const void *fn;
+    int threads;
     int blocks;
 };
-OccEntry g_occ[64];
-int g_occ_n = 0;
+constexpr int kOccSlots = 1024;  // more than twice the (kernel, block size) pairs queried
+OccEntry g_occ[kOccSlots];
 
-int blocks_per_sm(KernelFn fn, int threads) {
-    for (int i = 0; i < g_occ_n; ++i)
-        if (g_occ[i].fn == fn) return g_occ[i].blocks;
+// The slot holding (fn, threads), or the empty slot where it belongs (-1: full).
+int occ_slot(const void *fn, int threads) {
+    size_t h = ((reinterpret_cast<uintptr_t>(fn) >> 4) ^ static_cast<uintptr_t>(threads)) % kOccSlots;
+    for (int probe = 0; probe < kOccSlots; ++probe, h = (h + 1) % kOccSlots) {
+        if (g_occ[h].fn == nullptr || (g_occ[h].fn == fn && g_occ[h].threads == threads)) return static_cast<int>(h);
+    }
+    return -1;
+}
+
+template <typename Fn>
+int blocks_per_sm(Fn *fn, int threads) {
+    const void *f = reinterpret_cast<const void *>(fn);
+    const int h = occ_slot(f, threads);
+    if (h >= 0 && g_occ[h].fn == f) return g_occ[h].blocks;
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reinterpret_cast<const void *>(fn), threads, 0) !=
-            cudaSuccess ||
-        b < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, f, threads, 0) != cudaSuccess || b < 1) {
+        cudaGetLastError();
         b = 1;
-    if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{fn, b};
+    }
+    if (h >= 0) g_occ[h] = OccEntry{f, threads, b};
     return b;
+}
+
+// CTAs of a launch that the GPU holds from the start (its first wave), for
+// the L2 prefetch before the dependent-launch wait.  Makes no CUDA call, so
+// it is safe inside a stream capture: the cached occupancy when ar_init
+// queried it, else the bound that the SM's thread limit sets.
+template <typename Fn>
+int first_wave(Fn *fn, int threads, int sms) {
+    const void *f = reinterpret_cast<const void *>(fn);
+    const int h = occ_slot(f, threads);
+    const int per_sm = (h >= 0 && g_occ[h].fn == f) ? g_occ[h].blocks : 2048 / threads;
+    return per_sm * sms;
+}
+
+// Occupancy of every kernel a prefetching launch uses at its usual block
+// size, queried once (at ar_init, outside any stream capture).
+void warm_occupancy() {
+    const int dtypes[3] = {AR_F32, AR_F16, AR_BF16};
+    for (int dst : dtypes)
+        for (int wire : dtypes) {
+            const Kernels &k = kernels_for(dst, wire);
+            for (int nc = 0; nc < 2; ++nc) {
+                blocks_per_sm(k.v16.few[nc], kLatencyThreads);
+                blocks_per_sm(k.v16.many[nc], kLatencyThreads);
+                blocks_per_sm(k.bw16.few[nc], kBandwidthThreads);
+                blocks_per_sm(k.bw16.many[nc], kBandwidthThreads);
+                blocks_per_sm(k.wide.few[nc], kBandwidthThreads);
+                blocks_per_sm(k.wide.many[nc], kBandwidthThreads);
+                blocks_per_sm(k.pack[nc], 256);
+            }
+            if (k.pack32) blocks_per_sm(k.pack32, 256);
+            for (int many = 0; many < 2; ++many)
+                for (int res = 0; res < 2; ++res) {
+                    blocks_per_sm(k.ex[many][res][1], 256);
+                    if (k.ex32[many][res]) blocks_per_sm(k.ex32[many][res], 256);
+                }
+        }
 }
 
 int parse_variant(const char *s) {
@@ -228,7 +280,8 @@ int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t 
 
 // Launch one reduction; the caller holds g_mu and has validated the arguments.
 int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t nelem, int dst_dtype,
-                  int wire_dtype, int variant, int grid_blocks, cudaStream_t stream, bool explicit_variant) {
+                  int wire_dtype, int variant, int grid_blocks, cudaStream_t stream, bool explicit_variant,
+                  bool device_buffers = true) {
     Context &c = g_ctx;
     if (nelem == 0) return AR_OK;
 
@@ -278,6 +331,7 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     p.nelem = nelem;
     p.R = c.R;
     p.n_dsts = n_dsts;
+
 
     // A destination that is also a source is written while it is being
     // read, so those calls use coherent loads instead of the read-only path.
@@ -362,6 +416,11 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         const unsigned long long per_round = static_cast<unsigned long long>(grid) * threads;
         p.rounds = (nv + per_round - 1) / per_round;
         p.chunk = p.rounds ? (nv + p.rounds * grid - 1) / (p.rounds * grid) : 0;
+        // the first wave (the CTAs the GPU holds at once) prefetches its
+        // sources into L2 before waiting for the kernel ahead of it; device
+        // memory only: host buffers read over the CPU-GPU link are left to
+        // the loads
+        if (c.l2_prefetch && device_buffers) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
     }
     // The kernels wait (griddepcontrol.wait) for the kernel before them on
     // the stream before touching memory, so they may be launched as
@@ -413,7 +472,7 @@ int reduce_host_direct_locked(const void *const *h_srcs, void *const *h_dsts, in
     // one CTA per SM; buffers at different offsets from a vector boundary
     // fall back to the element-wise kernel on the same grid
     return launch_locked(s, d, n_dsts, nelem, dst_dtype, wire_dtype, AR_VARIANT_BANDWIDTH, c.sm_count, stream,
-                         false);
+                         false, false);
 }
 
 }  // namespace
@@ -505,7 +564,8 @@ int ar_init(int R, size_t max_elems) {
     };
     if (!env_int("AR_TMA_STAGES", 2, tps::kTmaMaxStages, &c.tma_stages) ||
         !env_int("AR_TMA_TILE", 1024, 32768, &c.tma_tile) || c.tma_tile % 1024 ||
-        !env_int("AR_TMA_CTAS_PER_SM", 1, 4, &c.tma_ctas_per_sm) || !env_int("AR_PDL", 0, 1, &c.pdl))
+        !env_int("AR_TMA_CTAS_PER_SM", 1, 4, &c.tma_ctas_per_sm) || !env_int("AR_PDL", 0, 1, &c.pdl) ||
+        !env_int("AR_L2_PREFETCH", 0, 1, &c.l2_prefetch))
         return AR_ERR_INVALID_ARG;
     if (const char *s = getenv("AR_LATENCY_MAX_BYTES")) {
         char *end = nullptr;
@@ -513,6 +573,7 @@ int ar_init(int R, size_t max_elems) {
         if (end == s || v < 0) return AR_ERR_INVALID_ARG;
         c.latency_max_bytes = v;
     }
+    warm_occupancy();
     if (!create_pipe(c.pipe)) return AR_ERR_CUDA;
     if (cudaMalloc(reinterpret_cast<void **>(&c.dev_status), 64) != cudaSuccess ||
         cudaMemset(c.dev_status, 0, 64) != cudaSuccess) {
@@ -849,6 +910,8 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     }
     if (gx < 1) gx = 1;
     const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
+    // the first wave prefetches its first row's operands into L2 before the wait
+    if (c.l2_prefetch && vec) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
     if (launch_dependent(fn, dim3(static_cast<unsigned>(gx), gy), static_cast<unsigned>(threads), 0, stream, c.pdl != 0,
                          p) != cudaSuccess) {
         cudaGetLastError();
@@ -903,8 +966,10 @@ int ar_wire_pack(const void *src, void *wire, size_t nelem, int dst_dtype, int w
     if (grid < 1) grid = 1;
     const void *s0 = static_cast<const char *>(src) + head * es;
     void *w0 = static_cast<char *>(wire) + head * ew;
+    const int prefetch_ctas = (c.l2_prefetch && vec) ? first_wave(fn, 256, c.sm_count) : 0;
     if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), 256u, 0, stream, g_ctx.pdl != 0, s0, w0,
-                         static_cast<unsigned long long>(nelem), static_cast<int>(head)) != cudaSuccess) {
+                         static_cast<unsigned long long>(nelem), static_cast<int>(head), prefetch_ctas) !=
+        cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
     }

@@ -20,7 +20,7 @@ struct VecKernels {
 
 using ExKernelFn = void (*)(ArExParams);
 using TmaKernelFn = void (*)(ArParams, TmaPlan);
-using PackKernelFn = void (*)(const void *, void *, unsigned long long, int);
+using PackKernelFn = void (*)(const void *, void *, unsigned long long, int, int);
 
 struct Kernels {
     ExKernelFn ex[2][2][2];  // [R >= 3][residual][16-byte vectors]

@@ -41,6 +41,11 @@ struct ArParams {
     // pointers forward to alignment and the first `head` elements sit at
     // indices -head .. -1.
     int head;
+    // CTAs 0 .. prefetch_ctas-1 (the ones resident from the start, so the
+    // ones that may run while the kernel ahead of this one on the stream is
+    // still draining) ask L2 for the source vectors of their first round
+    // before waiting for that kernel (see prefetch_first_round); 0 = none.
+    int prefetch_ctas;
 };
 
 // Programmatic dependent launch: when a launch opts in, the next kernel on
@@ -345,6 +350,34 @@ __device__ __forceinline__ void reduce_span(const ArParams &p, size_t first, siz
     }
 }
 
+// Ask L2 for the source vectors this thread loads in its first round (one
+// prefetch.global.L2 per rank), before pdl_wait.  Launched as a programmatic
+// dependent, the first wave of CTAs runs this while the kernel ahead of it on
+// the stream drains, so DRAM starts on this kernel's sources instead of
+// idling through the hand-over.  A prefetch returns no data: it only moves
+// lines into L2, the point where every write of the earlier kernel lands as
+// well, so a line it brings in is updated by any later write to it, and the
+// loads that use the data still come after pdl_wait.  Later waves start after
+// the hand-over and would only add a second request per load, so the host
+// limits the prefetch to the CTAs resident from the start.
+template <int VB, bool UNR>
+__device__ __forceinline__ void prefetch_first_round(const ArParams &p, size_t first, size_t end) {
+    const size_t idx = first + threadIdx.x;
+    if (idx >= end) return;
+    auto one = [&](int r) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.src[r]) + idx * VB));
+    };
+    if constexpr (UNR) {
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r >= p.R) break;
+            one(r);
+        }
+    } else {
+        for (int r = 0; r < p.R; ++r) one(r);
+    }
+}
+
 // The reduction kernel.  G CTAs of T threads cover nvec vectors of VB bytes
 // in K = ceil(nvec / (G*T*U)) rounds: in round k, CTA b takes the c vectors
 // starting at (k*G + b)*c, with c = ceil(nvec / (K*G)) <= T*U.  Launched
@@ -365,6 +398,8 @@ __global__ void __launch_bounds__(256) ar_reduce_kernel(const __grid_constant__ 
     const size_t G = gridDim.x;
     const size_t b = blockIdx.x;
     pdl_launch_dependents();
+    if (U == 1 && b < static_cast<size_t>(p.prefetch_ctas) && p.rounds > 0 && b * p.chunk < nvec)
+        prefetch_first_round<VB, UNR>(p, b * p.chunk, b * p.chunk + p.chunk < nvec ? b * p.chunk + p.chunk : nvec);
     pdl_wait();
     {
         const size_t K = p.rounds;  // ceil(nvec / (G * blockDim.x * U)), from the host

@@ -21,6 +21,7 @@ struct ArExParams {
     unsigned inactive;                // bit r: rank r contributes +0
     int R;
     int n_dsts;
+    int prefetch_ctas;                // CTAs (in launch order) that prefetch before the wait
 };
 
 // Operand r of element i of row `row`, rounded through the wire type; +0
@@ -65,6 +66,31 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
     pdl_launch_dependents();
+    if constexpr (VEC) {
+        // the first wave asks L2 for its first row's operands (as in
+        // ar_reduce_kernel's prefetch_first_round)
+        const size_t cta = static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t row = blockIdx.y;
+        if (cta < static_cast<size_t>(p.prefetch_ctas) && row < p.ne1) {
+            const unsigned off = static_cast<unsigned>(
+                (reinterpret_cast<uintptr_t>(p.dst[0]) + static_cast<long long>(row) * p.dst_stride[0]) % VB);
+            size_t h = off ? (VB - off) / Elem<Td>::bytes : 0;
+            if (h > p.ne0) h = p.ne0;
+            const size_t vpr = (p.ne0 - h) / V;
+            const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+            const size_t at = h * Elem<Td>::bytes + v * VB;
+            if (v < vpr) {
+                for (int r = 0; r < p.R; ++r)
+                    if (!((p.inactive >> r) & 1u))
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.src[r]) +
+                                                                      static_cast<long long>(row) * p.src_stride[r] +
+                                                                      at));
+                if constexpr (RES)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.residual) +
+                                                                  static_cast<long long>(row) * p.res_stride + at));
+            }
+        }
+    }
     pdl_wait();  // the kernel before this one on the stream has finished
     for (size_t row = blockIdx.y; row < p.ne1; row += gridDim.y) {
         if constexpr (VEC) {
@@ -174,7 +200,7 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
 // eight elements in flight per thread.
 template <int Td, int Tw, bool VEC, int VB = 16>
 __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wire, unsigned long long nelem,
-                                                      int head) {
+                                                      int head, int prefetch_ctas) {
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
     constexpr int WB = V * Elem<Tw>::bytes;  // output bytes per vector: 8, 16 or 32
@@ -188,6 +214,12 @@ __global__ void __launch_bounds__(256) ar_pack_kernel(const void *src, void *wir
     };
     auto one = [&](long long i) { put(i, load_elem<Td, false>(src, i)); };
     pdl_launch_dependents();
+    if constexpr (VEC) {
+        // the first wave asks L2 for its source vector before the wait
+        const size_t v = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (blockIdx.x < static_cast<unsigned>(prefetch_ctas) && v < nelem / V)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(src) + v * VB));
+    }
     pdl_wait();  // the kernel before this one on the stream has finished
     if constexpr (VEC) {
         const size_t nvec = nelem / V;

@@ -345,3 +345,41 @@ def test_more_rows_than_the_grid_holds(ne0, pad):
     differing strides) cover every row."""
     run_ex(2, ne0, 70_001, "f32", "bf16", seed=ne0, src_pad=[pad, 2 * pad], dst_pad=(0,), residual=True,
            res_pad=0)
+
+
+@pytest.mark.parametrize("prefetch", ["0", "1"])
+def test_chained_in_place_updates_and_pack_see_the_previous_results(prefetch, monkeypatch):
+    """x = x + reduce(partials_k) four times in place into the residual (the
+    destination is the residual), then the wire pack of the result, all back
+    to back on one created stream inside a CUDA graph: each launch is a
+    programmatic dependent of the one before, whose output it reads, and
+    (AR_L2_PREFETCH=1, the default) asks L2 for its operands before waiting
+    for it.  Every step must read the previous step's final bits."""
+    monkeypatch.setenv("AR_L2_PREFETCH", prefetch)
+    ne0, ne1, R, steps = 4096, 1024, 2, 4
+    n = ne0 * ne1
+    tps.ar_init(R, n)
+    x0 = srcs_for(7 + int(prefetch), 1, n, "f32")[0]
+    parts = [srcs_for(100 * k + int(prefetch), R, n, "f32") for k in range(steps)]
+    exp = x0
+    for k in range(steps):
+        exp = oracle.reduce_2d(parts[k], 1, "f32", "bf16", ne0, ne1, residual=exp)[0]
+    exp_pack = oracle.wire_pack(exp, "f32", "bf16")
+    x = to_device(x0, "f32")
+    d_parts = [[to_device(a, "f32") for a in p] for p in parts]
+    wire = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    lay = tps.make_layout(ne0, ne1, residual=x)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(steps):
+            tps.ar_reduce_ex(d_parts[k], [x], lay, "f32", "bf16", stream=stream)
+        tps.ar_wire_pack(x, wire, dst_dtype="f32", wire_dtype="bf16", stream=stream)
+    x.copy_(to_device(x0, "f32"))
+    wire.view(torch.int16).fill_(0x7FC1)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same(to_host(x, "f32"), exp, "f32", f"in-place chain AR_L2_PREFETCH={prefetch}")
+    assert_same(to_host(wire, "bf16"), exp_pack, "bf16", f"pack after the chain AR_L2_PREFETCH={prefetch}")

@@ -695,6 +695,47 @@ def test_plain_and_dependent_launches_give_the_same_bits(ctx, pdl, monkeypatch):
             assert_same(to_host(d, "f32"), exp, "f32", f"AR_PDL={pdl} variant={v}")
 
 
+@pytest.mark.parametrize("prefetch", ["0", "1"])
+@pytest.mark.parametrize("n", [100_003, 3_000_017])  # the latency and the bandwidth launch
+def test_chained_reductions_see_the_previous_results(ctx, prefetch, n, monkeypatch):
+    """Each reduction sums the previous one's output with a new partial; the
+    six launches run back to back on one created stream inside a CUDA graph,
+    each a programmatic dependent of the one before, which (AR_L2_PREFETCH=1,
+    the default) asks L2 for its sources before it waits for that kernel.
+    Every step must read the previous step's final bits: the chain equals the
+    oracle's chain, with the prefetch on and off."""
+    monkeypatch.setenv("AR_L2_PREFETCH", prefetch)
+    tps.ar_init(2, n)
+    ctx.R = None  # the next test re-initialises with its own limits (and without the variable)
+    steps = 6
+    parts = srcs_for(n + int(prefetch), steps + 1, n, "f32")
+    exp, prev = [], parts[0]
+    for k in range(1, steps + 1):
+        prev = expect([prev, parts[k]], "f32", "bf16")
+        exp.append(prev)
+    d_parts = [to_device(a, "f32") for a in parts]
+    outs = [torch.empty(n, device="cuda") for _ in range(steps)]
+    stream = torch.cuda.Stream()
+
+    def chain(s):
+        src = d_parts[0]
+        for k in range(steps):
+            tps.ar_reduce([src, d_parts[k + 1]], [outs[k]], dst_dtype="f32", wire_dtype="bf16", stream=s)
+            src = outs[k]
+
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain(stream)
+    for o in outs:
+        o.view(torch.int32).fill_(0x7FC00001)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in range(steps):
+        assert_same(to_host(outs[k], "f32"), exp[k], "f32", f"step {k + 1} AR_L2_PREFETCH={prefetch}")
+
+
 @pytest.mark.parametrize("variant", ["auto", "latency", "bandwidth", "scalar"])
 def test_prepared_call_gives_the_same_bits(ctx, variant):
     n = 50_003
