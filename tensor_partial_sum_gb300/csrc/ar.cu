@@ -332,7 +332,6 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
     p.R = c.R;
     p.n_dsts = n_dsts;
 
-
     // A destination that is also a source is written while it is being
     // read, so those calls use coherent loads instead of the read-only path.
     const int nc = alias ? 0 : 1;

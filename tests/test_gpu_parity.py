@@ -415,6 +415,27 @@ def test_host_entry_direct(ctx, dst, wire, R, n):
         assert_same(h.numpy().view(np.uint32 if dst == "f32" else np.uint16), exp, dst, "direct host")
 
 
+@pytest.mark.parametrize("n", [4099, 3_000_017])  # the latency and the bandwidth launch
+def test_device_entry_point_on_pinned_host_memory(ctx, n):
+    """ar_reduce given pinned host buffers as its device pointers (the GPU
+    reaches them over the CPU-GPU link): two calls back to back on a created
+    stream, so the second launches as a programmatic dependent and its first
+    wave prefetches before it waits; both give the oracle's bits."""
+    R = 3
+    ctx.ensure(R, n)
+    srcs = srcs_for(n + 5, R, n, "f32")
+    exp = expect(srcs, "f32", "bf16")
+    h_srcs = [torch.from_numpy(s).pin_memory() for s in srcs]
+    h_dsts = [torch.full((n,), float("nan")).pin_memory() for _ in range(2)]
+    stream = torch.cuda.Stream()
+    for k in range(2):
+        tps.ar_reduce_variant([h.data_ptr() for h in h_srcs], [h_dsts[k].data_ptr()], "auto", nelem=n,
+                              dst_dtype="f32", wire_dtype="bf16", stream=stream)
+    stream.synchronize()
+    for h in h_dsts:
+        assert_same(h.numpy(), exp, "f32", f"pinned host buffers n={n}")
+
+
 @pytest.mark.parametrize("offsets,want", [((1, 1, 1), "bandwidth"), ((1, 2, 3), "scalar")])
 def test_host_entry_direct_unaligned_and_in_place(ctx, offsets, want):
     """Pinned buffers off 16-byte alignment: one shared offset keeps the
