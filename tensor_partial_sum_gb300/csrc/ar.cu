@@ -28,7 +28,7 @@ namespace {
 constexpr int kLatencyThreads = 128;
 constexpr int kBandwidthThreads = 256;
 constexpr int kScalarThreads = 256;
-constexpr int64_t kDefaultLatencyMaxBytes = 32ll << 20;  // measured crossover on GB300
+constexpr int64_t kDefaultLatencyMaxBytes = 16ll << 20;  // measured crossover on GB300
 // ar_reduce_host cuts a call into chunks of this many bytes per buffer (at
 // most kMaxHostChunks chunks) so that host->device copies, kernels and
 // device->host copies of different chunks overlap.
@@ -182,6 +182,7 @@ void warm_occupancy() {
                 blocks_per_sm(k.wide.few[nc], kBandwidthThreads);
                 blocks_per_sm(k.wide.many[nc], kBandwidthThreads);
                 blocks_per_sm(k.pack[nc], 256);
+                blocks_per_sm(k.scalar[nc], kScalarThreads);
             }
             if (k.pack32) blocks_per_sm(k.pack32, 256);
             for (int many = 0; many < 2; ++many)
@@ -269,7 +270,9 @@ int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t 
     long long grid = grid_blocks > 0 ? grid_blocks : static_cast<long long>(c.sm_count) * c.tma_ctas_per_sm;
     if (grid > static_cast<long long>(plan.ntiles)) grid = static_cast<long long>(plan.ntiles);
     if (grid < 1) grid = 1;
-    if (launch_dependent(k.tma, dim3(static_cast<unsigned>(grid)), tps::kTmaThreads, smem, stream, c.pdl != 0, p,
+    ArParams pt = p;  // every CTA of the persistent grid is resident from the start
+    pt.prefetch_ctas = c.l2_prefetch ? static_cast<int>(grid) : 0;
+    if (launch_dependent(k.tma, dim3(static_cast<unsigned>(grid)), tps::kTmaThreads, smem, stream, c.pdl != 0, pt,
                          plan) != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
@@ -395,6 +398,8 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
             threads = kScalarThreads;
             const long long cap = grid_blocks > 0 ? grid_blocks : sms * blocks_per_sm(fn, threads);
             grid = grid_cap(grid_blocks > 0 ? cap : (static_cast<long long>(nelem) + threads - 1) / threads, cap);
+            // the first wave prefetches its first elements before the wait
+            if (c.l2_prefetch && device_buffers) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
             break;
         }
         case AR_VARIANT_TMA:

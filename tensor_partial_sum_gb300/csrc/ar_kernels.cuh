@@ -435,8 +435,18 @@ __global__ void __launch_bounds__(256) ar_scalar_kernel(const __grid_constant__ 
     constexpr int RB = 4;
     const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
     pdl_launch_dependents();
-    pdl_wait();
     size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (blockIdx.x < static_cast<unsigned>(p.prefetch_ctas)) {
+        // the first iteration's elements into L2 before the wait (as in
+        // prefetch_first_round)
+        for (int r = 0; r < p.R; ++r)
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (i + e * step < p.nelem)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.src[r]) +
+                                                                  (i + e * step) * Elem<Td>::bytes));
+    }
+    pdl_wait();
     for (; i + (E - 1) * step < p.nelem; i += E * step) {
         float acc[E];
 #pragma unroll

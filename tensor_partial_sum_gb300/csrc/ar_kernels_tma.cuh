@@ -99,6 +99,23 @@ __global__ void __launch_bounds__(kTmaThreads) ar_tma_kernel(const __grid_consta
                                                                 const __grid_constant__ TmaPlan plan) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_launch_dependents();
+    if (threadIdx.x < static_cast<unsigned>(p.R) && blockIdx.x < static_cast<unsigned>(p.prefetch_ctas)) {
+        // the first stages' tiles of rank threadIdx.x into L2 while the
+        // kernel ahead drains (a prefetch returns no data, so the bulk loads
+        // after the wait still see that kernel's writes); tiles start on
+        // 1 KiB boundaries of 16-byte aligned buffers and span whole vectors
+        for (unsigned k = 0; k < plan.stages; ++k) {
+            const unsigned long long t = blockIdx.x + static_cast<unsigned long long>(k) * gridDim.x;
+            if (t >= plan.ntiles) break;
+            const unsigned long long off = t * plan.tile_bytes;
+            const unsigned bytes =
+                static_cast<unsigned>(min(static_cast<unsigned long long>(plan.tile_bytes), plan.vec_bytes - off));
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char *>(
+                             p.src[threadIdx.x]) + off),
+                         "r"(bytes)
+                         : "memory");
+        }
+    }
     pdl_wait();  // the kernel before this one on the stream has finished
     unsigned long long *full = reinterpret_cast<unsigned long long *>(smem);
     unsigned long long *empty = full + kTmaMaxStages;
