@@ -42,7 +42,7 @@
  *   - Calls that take a stream only enqueue work on it and return; results
  *     are ready when the stream reaches that point.  No call synchronizes
  *     (a host call given pageable memory waits for CUDA's synchronous
- *     pageable copies, see ar_reduce_host_noalloc), so ar_reduce and
+ *     pageable copies, see ar_reduce_host and ar_reduce_host_noalloc), so ar_reduce and
  *     ar_reduce_variant can be captured in a CUDA graph.
  *   - On any status other than AR_OK nothing has been enqueued or written,
  *     except AR_ERR_CUDA from a launch, after which the stream's state is
@@ -221,7 +221,12 @@ int ar_set_option(int key, int64_t value);
  *                   AR_Q_HOST_CHUNK_BYTES) and pipelined over three streams
  *                   the context owns, so copies in, kernels and copies out of
  *                   different chunks overlap.  Pinned host memory makes the
- *                   copies asynchronous; pageable memory also works.
+ *                   copies asynchronous; pageable memory also works, but CUDA
+ *                   copies it synchronously, so the call then waits for its
+ *                   copies.  It waits without holding the library lock:
+ *                   other threads' calls go on, except another staged
+ *                   ar_reduce_host (the pipeline is one per context) and
+ *                   ar_init / ar_free, which wait for this call to end.
  *   both NULL       no staging: the kernel itself loads the host partials and
  *                   stores the host results over the CPU-GPU link (NVLink-C2C
  *                   on GB300), with no copies at all.  Every host buffer must

@@ -92,6 +92,10 @@ bool create_pipe(HostPipe &p) {
 
 std::mutex g_mu;
 Context g_ctx;
+// Held by a staged ar_reduce_host for its whole call (the context's pipeline
+// streams and events are one set), and by ar_init and ar_free while they
+// replace the context.  Lock order: g_pipe_mu before g_mu.
+std::mutex g_pipe_mu;
 // Incremented (under g_mu) by every ar_init and ar_free: a call that drops
 // the lock half way through can tell whether the context was replaced.
 unsigned long long g_ctx_gen = 0;
@@ -535,6 +539,7 @@ int ar_init(int R, size_t max_elems) {
     const int variant = parse_variant(getenv("AR_VARIANT"));
     if (variant < 0) return AR_ERR_INVALID_ARG;
 
+    std::lock_guard<std::mutex> pipe_lock(g_pipe_mu);
     std::lock_guard<std::mutex> lock(g_mu);
     destroy_pipe(g_ctx.pipe);
     if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
@@ -594,6 +599,7 @@ int ar_init(int R, size_t max_elems) {
 }
 
 void ar_free(void) {
+    std::lock_guard<std::mutex> pipe_lock(g_pipe_mu);
     std::lock_guard<std::mutex> lock(g_mu);
     destroy_pipe(g_ctx.pipe);
     if (g_ctx.dev_status) cudaFree(g_ctx.dev_status);
@@ -683,37 +689,53 @@ int ar_set_option(int key, int64_t value) {
 
 int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, size_t nelem, int dst_dtype,
                    int wire_dtype, void *const *d_srcs, void *const *d_dsts, cudaStream_t stream) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
-    const Context &c = g_ctx;
-    if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
-    if (!d_srcs != !d_dsts) return AR_ERR_INVALID_ARG;
-    if (!d_srcs) return reduce_host_direct_locked(h_srcs, h_dsts, n_dsts, nelem, dst_dtype, wire_dtype, stream);
-    const void *srcs_c[AR_MAX_RANKS];
-    for (int r = 0; r < c.R; ++r) srcs_c[r] = d_srcs[r];
-    int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
-    if (st != AR_OK) return st;
-    if (nelem == 0) return AR_OK;
-    // The host buffers obey the same rules.  A host destination that partly
-    // overlaps a host source would be written (copy back of chunk k) before
-    // a later chunk's copy in has read the source bytes it shares.
-    st = ar_check_args(c.R, h_srcs, h_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
-    if (st != AR_OK) return st;
-    {  // the launch below checks the device too, but only after copies would be queued
+    if (!d_srcs && !d_dsts) {  // direct mode: one launch, under the library lock like every launch
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+        if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
+        return reduce_host_direct_locked(h_srcs, h_dsts, n_dsts, nelem, dst_dtype, wire_dtype, stream);
+    }
+    // Staged mode.  g_pipe_mu gives this call the context's pipeline streams
+    // and events (and keeps them alive: ar_init and ar_free take it too).
+    // The copies are enqueued without g_mu, because a copy from or to
+    // pageable host memory can block the calling thread until its stream
+    // gets there, and other library calls must not wait behind it; each
+    // chunk's launch takes g_mu.
+    std::lock_guard<std::mutex> pipe_lock(g_pipe_mu);
+    int R = 0;
+    size_t chunk = 0;
+    HostPipe pp;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_ctx.ready) return AR_ERR_NOT_INITIALIZED;
+        const Context &c = g_ctx;
+        if (!h_srcs || !h_dsts) return AR_ERR_INVALID_ARG;
+        if (!d_srcs || !d_dsts) return AR_ERR_INVALID_ARG;
+        const void *srcs_c[AR_MAX_RANKS];
+        for (int r = 0; r < c.R; ++r) srcs_c[r] = d_srcs[r];
+        int st = ar_check_args(c.R, srcs_c, d_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+        if (st != AR_OK) return st;
+        if (nelem == 0) return AR_OK;
+        // The host buffers obey the same rules.  A host destination that partly
+        // overlaps a host source would be written (copy back of chunk k) before
+        // a later chunk's copy in has read the source bytes it shares.
+        st = ar_check_args(c.R, h_srcs, h_dsts, n_dsts, nelem, c.max_elems, dst_dtype, wire_dtype);
+        if (st != AR_OK) return st;
+        // the launches check the device too, but only after copies would be queued
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
         if (dev != c.device) return AR_ERR_INVALID_ARG;
+        if (c.fault_inject) return AR_ERR_CUDA;
+        // Chunks of whole 256-element groups (so every chunk keeps the buffers'
+        // alignment); chunking never changes a result bit.
+        chunk = static_cast<size_t>(c.host_chunk_bytes) / elem_bytes(dst_dtype);
+        const size_t min_chunk = (nelem + kMaxHostChunks - 1) / kMaxHostChunks;
+        if (chunk < min_chunk) chunk = min_chunk;
+        chunk = (chunk + 255) / 256 * 256;
+        R = c.R;
+        pp = c.pipe;
     }
-    if (c.fault_inject) return AR_ERR_CUDA;
-
-    // Chunks of whole 256-element groups (so every chunk keeps the buffers'
-    // alignment); chunking never changes a result bit.
     const size_t esize = elem_bytes(dst_dtype);
-    size_t chunk = static_cast<size_t>(c.host_chunk_bytes) / esize;
-    const size_t min_chunk = (nelem + kMaxHostChunks - 1) / kMaxHostChunks;
-    if (chunk < min_chunk) chunk = min_chunk;
-    chunk = (chunk + 255) / 256 * 256;
-    const HostPipe &pp = c.pipe;
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
     // everything the caller enqueued on `stream` before this call comes first
     if (!ok(cudaEventRecord(pp.start, stream)) || !ok(cudaStreamWaitEvent(pp.h2d, pp.start, 0)) ||
@@ -725,7 +747,7 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
     for (size_t off = 0; off < nelem; off += chunk, ++k) {
         const size_t n = nelem - off < chunk ? nelem - off : chunk;
         const size_t boff = off * esize, nb = n * esize;
-        for (int r = 0; r < c.R; ++r) {
+        for (int r = 0; r < R; ++r) {
             char *dptr = static_cast<char *>(d_srcs[r]) + boff;
             if (!ok(cudaMemcpyAsync(dptr, static_cast<const char *>(h_srcs[r]) + boff, nb, cudaMemcpyHostToDevice,
                                     pp.h2d)))
@@ -735,8 +757,12 @@ int ar_reduce_host(const void *const *h_srcs, void *const *h_dsts, int n_dsts, s
         for (int d = 0; d < n_dsts; ++d) cd[d] = static_cast<char *>(d_dsts[d]) + boff;
         if (!ok(cudaEventRecord(pp.copied[k], pp.h2d)) || !ok(cudaStreamWaitEvent(pp.comp, pp.copied[k], 0)))
             return AR_ERR_CUDA;
-        const int lst = launch_locked(cs, cd, n_dsts, n, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, pp.comp, false);
-        if (lst != AR_OK) return lst;
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            const int lst =
+                launch_locked(cs, cd, n_dsts, n, dst_dtype, wire_dtype, AR_VARIANT_AUTO, 0, pp.comp, false);
+            if (lst != AR_OK) return lst;
+        }
         if (!ok(cudaEventRecord(pp.reduced[k], pp.comp)) || !ok(cudaStreamWaitEvent(pp.d2h, pp.reduced[k], 0)))
             return AR_ERR_CUDA;
         for (int d = 0; d < n_dsts; ++d)

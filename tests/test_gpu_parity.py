@@ -512,6 +512,58 @@ def test_concurrent_calls_from_two_threads(ctx):
         assert_same(to_host(out, "f32"), exp, "f32", "concurrent")
 
 
+def test_host_calls_with_pageable_memory_beside_device_calls(ctx):
+    """Three threads at once: two run staged ar_reduce_host calls on pageable
+    (numpy) buffers, whose copies block the calling thread, each on its own
+    stream and staging buffers; the third runs ar_reduce on device buffers.
+    The staged calls take turns on the pipeline, nothing deadlocks, and every
+    result is right."""
+    import threading
+    R, n = 3, 300_007
+    ctx.ensure(R, n)
+    errors, host_cases = [], []
+    for k in range(2):
+        srcs = srcs_for(700 + k, R, n, "f32")
+        host_cases.append((srcs, expect(srcs, "f32", "bf16"), [np.full(n, np.nan, np.float32) for _ in range(2)],
+                           [torch.empty(n, device="cuda") for _ in range(R)],
+                           [torch.empty(n, device="cuda") for _ in range(2)], torch.cuda.Stream()))
+    dsrcs = srcs_for(709, R, n, "f32")
+    dexp = expect(dsrcs, "f32", "bf16")
+    d_t = [to_device(a, "f32") for a in dsrcs]
+    d_out = torch.empty(n, device="cuda")
+    d_stream = torch.cuda.Stream()
+
+    def host_worker(k):
+        try:
+            srcs, _, outs, ds, dd, stream = host_cases[k]
+            for _ in range(10):
+                tps.ar_reduce_host(srcs, outs, ds, dd, nelem=n, dst_dtype="f32", wire_dtype="bf16", stream=stream)
+            stream.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    def device_worker():
+        try:
+            for _ in range(200):
+                tps.ar_reduce(d_t, [d_out], dst_dtype="f32", wire_dtype="bf16", stream=d_stream)
+            d_stream.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=host_worker, args=(k,)) for k in range(2)]
+    threads.append(threading.Thread(target=device_worker))
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not any(t.is_alive() for t in threads), "a thread did not finish"
+    assert not errors, errors
+    for _, exp, outs, _, _, _ in host_cases:
+        for o in outs:
+            assert_same(o, exp, "f32", "staged, pageable, from a thread")
+    assert_same(to_host(d_out, "f32"), dexp, "f32", "device calls beside host calls")
+
+
 @pytest.mark.parametrize("wire", ["bf16", "f16"])
 def test_kernel_casts_exhaustive(ctx, wire):
     """Every float32 bit pattern through the kernel with R = 1 (the wire
