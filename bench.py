@@ -221,6 +221,14 @@ def gpu_id_for(device_index: int) -> str:
         return vis.split(",")[device_index] if vis else str(device_index)
 
 
+def launch_mode() -> str:
+    """How the library launches its kernels, from the environment it reads at ar_init."""
+    pdl = os.environ.get("AR_PDL", "1") != "0"
+    pf = os.environ.get("AR_L2_PREFETCH", "1") != "0"
+    return ("programmatic dependent launches" if pdl else "plain launches") + \
+        (", first wave prefetches its sources into L2 before the wait" if pf else ", no L2 prefetch")
+
+
 def config_steps(w, steps: int, group: int, min_seconds: float = 2e-3) -> int:
     """Timed launches for a workload measured beside the headline: at least
     ``steps``, enough for about ``min_seconds`` of GPU time at the HBM peak
@@ -584,7 +592,7 @@ def run_ours(args):
         "accumulate": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.describe()}", "bytes_per_step": w.bytes_per_call,
                    "variant": m["variant"], "parallelism": f"{run.world} independent replica(s), no collective",
-                   "l2": m["l2"], "timing": m["timing"]},
+                   "l2": m["l2"], "timing": m["timing"], "launch": launch_mode()},
         "roofline": roof,
         "gpu_launches": args.steps,
         "clocks": m["clocks"],
@@ -741,7 +749,8 @@ def run_reference(args):
                    "variant": "oracle (scalar C, element by element)",
                    "parallelism": "oracle on rank 0 only, contiguous row ranges on every host core",
                    "l2": "host caches; each step is a bounded sample of the workload's rows",
-                   "timing": "wall clock (time.perf_counter) around the timed steps"},
+                   "timing": "wall clock (time.perf_counter) around the timed steps",
+                   "launch": "none: the oracle runs on the host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": nt, "kind": "oracle", "sample": text,
                          "machine": platform.machine()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
