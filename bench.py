@@ -44,9 +44,11 @@ FALLBACK_HBM_GBS = 6800.0
 # the HBM3e bandwidth the roofline is usually quoted against (GB300, ~8 TB/s)
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-# the file that defines the timed kernel (ar_reduce_kernel) and its helpers: a launch's
-# traffic depends on this code, not on the host code or the other kernels
-KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", "ar_kernels.cuh")]
+# the file that defines the timed kernel (ar_reduce_kernel) and its helpers, and the table
+# of its instantiations: a launch's traffic depends on this code, not on the rest of the
+# host code or the other kernels
+KERNEL_SOURCES = [os.path.join(ROOT, "tensor_partial_sum_gb300", "csrc", f)
+                  for f in ("ar_kernels.cuh", "ar_dispatch.h")]
 # GPU clock cycles of idle work enqueued ahead of the start event (about 0.2 ms)
 LEAD_CYCLES = 400_000
 # the workloads the benchmark is specified on, in their order, with the class each is judged as
