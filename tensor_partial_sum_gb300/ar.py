@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libtps_ar.so")
@@ -53,7 +54,9 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(f"{_LIB_PATH} is not built: run `python -m tensor_partial_sum_gb300.build`")
         L = ctypes.CDLL(_LIB_PATH)
         vp, sz, i, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
-        pp = ctypes.POINTER(ctypes.c_void_p)
+        # pointer arrays travel as packed bytes (see _ptrs): the C side reads
+        # R or n_dsts 64-bit addresses from the buffer
+        pp = ctypes.c_char_p
         L.ar_init.argtypes = [i, sz]
         L.ar_init.restype = i
         L.ar_reduce.argtypes = [pp, pp, i, sz, i, i, vp]
@@ -102,15 +105,20 @@ def _ptr(x) -> int | None:
 AR_MAX_RANKS = 16
 
 
+_PTR_ARRAY = struct.Struct(f"={AR_MAX_RANKS}Q")
+
+
 def _ptrs(xs):
-    """Pointer array padded with NULLs to at least AR_MAX_RANKS entries, so
-    a list shorter than the context's R is rejected (NULL source) instead of
-    being read past its end."""
+    """Pointer array (packed native 64-bit addresses, 0 for None) padded to
+    at least AR_MAX_RANKS entries, so a list shorter than the context's R is
+    rejected (NULL source) instead of being read past its end.  Packing with
+    struct costs a fraction of building a ctypes array of c_void_p."""
     if xs is None:
         return None
-    ptrs = [_ptr(x) for x in xs]
-    ptrs += [None] * max(0, AR_MAX_RANKS - len(ptrs))
-    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+    ptrs = [_ptr(x) or 0 for x in xs]
+    if len(ptrs) <= AR_MAX_RANKS:
+        return _PTR_ARRAY.pack(*ptrs, *([0] * (AR_MAX_RANKS - len(ptrs))))
+    return struct.pack(f"={len(ptrs)}Q", *ptrs)
 
 
 ESIZE = {AR_F32: 4, AR_F16: 2, AR_BF16: 2}

@@ -70,3 +70,19 @@ def test_prepared_call_checks_its_buffers_once():
     a = torch.zeros(64)
     with pytest.raises(TypeError, match="cpu tensor"):
         tps.PreparedReduce([a, a], [a.clone()])
+
+
+def test_pointer_arrays_are_packed_addresses():
+    """Pointer arrays reach the library as native 64-bit addresses, padded
+    with NULLs to 16 entries (so a short list reads as a NULL source, which
+    the library refuses, instead of memory past the list)."""
+    import struct
+    from tensor_partial_sum_gb300 import ar
+    packed = ar._ptrs([0x1000, None, 0xFFFFFFFFFFFFFFF0])
+    assert len(packed) == 16 * 8
+    vals = struct.unpack("=16Q", packed)
+    assert vals[:3] == (0x1000, 0, 0xFFFFFFFFFFFFFFF0) and vals[3:] == (0,) * 13
+    assert ar._ptrs(None) is None
+    assert len(ar._ptrs(list(range(1, 18)))) == 17 * 8
+    a = np.zeros(4, np.float32)
+    assert struct.unpack("=16Q", ar._ptrs([a]))[0] == a.ctypes.data
