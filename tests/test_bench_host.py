@@ -116,3 +116,12 @@ def test_oracle_rate_reports_its_threads():
     w = W.WORKLOADS["tp_small"]
     v, el, text = bench.oracle_rate(W.generate(w), w, 0.2, steps=2, threads=2)
     assert v > 0 and el > 0 and "on 2 thread(s)" in text
+
+
+def test_launch_mode_follows_the_library_environment(monkeypatch):
+    monkeypatch.delenv("AR_PDL", raising=False)
+    monkeypatch.delenv("AR_L2_PREFETCH", raising=False)
+    assert bench.launch_mode().startswith("programmatic dependent launches, first wave prefetches")
+    monkeypatch.setenv("AR_PDL", "0")
+    monkeypatch.setenv("AR_L2_PREFETCH", "0")
+    assert bench.launch_mode() == "plain launches, no L2 prefetch"
