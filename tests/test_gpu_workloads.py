@@ -67,6 +67,26 @@ def test_full_size_workload(name):
         assert_same(to_host(t, w.dst), exp, w.dst, f"{name} destination {d}, all {w.nelem} elements")
 
 
+@pytest.mark.parametrize("dst,wire", [(d, w) for d in ("f32", "f16", "bf16") for w in ("f32", "f16", "bf16")])
+def test_every_dtype_pair_at_prefill_size(dst, wire):
+    """Every (T_dst, T_wire) pair at the prefill shape (R=2 [2048,4096], 2
+    destinations) on edge-laden inputs (normals, f16-overflowing values,
+    subnormals, signed zeros, infinities, NaN, ties), launched as the
+    benchmark launches; every element compared with the oracle."""
+    from tests.libcasts import lib_round
+    from tests.test_oracle_fold import edgy_f32
+    n = 2048 * 4096
+    rng = np.random.Generator(np.random.PCG64(4096 + len(dst) * 7 + len(wire)))
+    srcs = [lib_round(dst, edgy_f32(rng, n)) for _ in range(2)]
+    tps.ar_init(2, n)
+    src_t = [to_device(a, dst) for a in srcs]
+    dst_t = [torch.empty(n, dtype=TORCH_DTYPE[dst], device="cuda") for _ in range(2)]
+    as_benchmarked(lambda s: tps.ar_reduce(src_t, dst_t, nelem=n, dst_dtype=dst, wire_dtype=wire, stream=s), dst_t)
+    exp = whole.reduce(srcs, dst, wire)
+    for d, t in enumerate(dst_t):
+        assert_same(to_host(t, dst), exp, dst, f"{dst}/{wire} destination {d}, all {n} elements")
+
+
 def test_decode_every_call_graph_captured():
     """The decode workload exactly as benchmarked: 10000 calls with their own
     buffers captured in one CUDA graph; every output element of every call is
