@@ -98,7 +98,7 @@ typedef enum {
     AR_VARIANT_SCALAR = 4,    /* element-wise path used when the buffers' offsets differ */
     AR_VARIANT_TMA = 5        /* shared-memory staging: a producer warp bulk-copies (cp.async.bulk)
                                  R source tiles per stage, sixteen warps fold them, one thread
-                                 bulk-stores the result tile to every destination; one CTA per SM.
+                                 bulk-stores the result tile to every destination; two CTAs per SM.
                                  Needs 16-byte aligned buffers.  Never chosen by AUTO (an
                                  AR_VARIANT environment override with offset buffers takes
                                  BANDWIDTH, or SCALAR when the offsets differ).  Its internal waits are bounded: a wait
@@ -114,7 +114,7 @@ typedef enum {
  * scalar|tma), AR_LATENCY_MAX_BYTES (size switch, bytes of sources plus
  * destinations), AR_TMA_STAGES (2..8, default 3), AR_TMA_TILE (largest
  * tile in bytes, a multiple of 1024 up to 32768, default 16384),
- * AR_TMA_CTAS_PER_SM (1..4, default 1), AR_PDL (1 = default: on a created
+ * AR_TMA_CTAS_PER_SM (1..4, default 2), AR_PDL (1 = default: on a created
  * stream, every kernel but NAIVE's launches as a programmatic dependent of
  * the kernel before it on the stream, which it waits for before touching
  * memory; launches on the default streams stay plain; 0 = plain launches

@@ -59,7 +59,7 @@ struct Context {
     unsigned *dev_status = nullptr;  // device word the TMA variant sets when a wait runs out
     int tma_stages = 3;              // AR_TMA_STAGES (2..8)
     int tma_tile = 16384;            // AR_TMA_TILE: largest tile, bytes (1024 .. 32768, 1 KiB multiples)
-    int tma_ctas_per_sm = 1;         // AR_TMA_CTAS_PER_SM (1..4)
+    int tma_ctas_per_sm = 2;         // AR_TMA_CTAS_PER_SM (1..4)
     int64_t tma_drop_tile = -1;      // test hook (AR_Q_TMA_DROP_TILE), -1 = off
     int pdl = 1;                     // AR_PDL: kernels launch as programmatic dependents
     int l2_prefetch = 1;             // AR_L2_PREFETCH: the first wave prefetches its sources before the wait
@@ -247,8 +247,8 @@ int grid_cap(long long want, long long cap) {
 }
 
 // TMA variant: 3 stages of R source tiles plus two output tiles in shared
-// memory, the tile as large as fits (1 KiB multiples, at most 16 KiB), one
-// CTA per SM (or grid_blocks), every wait bounded by 100 ms.
+// memory, the tile as large as fits (1 KiB multiples, at most 16 KiB), two
+// CTAs per SM (or grid_blocks), every wait bounded by 100 ms.
 constexpr size_t kTmaSmemBudget = 224 * 1024;  // per SM
 
 int launch_tma_locked(const Kernels &k, const ArParams &p, size_t nelem, size_t esize, int grid_blocks,
