@@ -30,6 +30,20 @@ def test_header_is_c11_and_host_calls_work(tmp_path):
     assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
 
 
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_layout_struct_matches_the_binding(tmp_path):
+    """ar_layout as a C compiler lays it out from the header has the size and
+    field offsets of the binding's ctypes mirror (ArLayout)."""
+    import ctypes
+    from tensor_partial_sum_gb300 import ar as A
+    exe = _compile("layout_offsets.c", str(tmp_path / "layout_offsets"))
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    c = {k: int(v) for k, v in (line.split() for line in out.stdout.splitlines())}
+    assert c.pop("size") == ctypes.sizeof(A.ArLayout)
+    assert c == {name: getattr(A.ArLayout, name).offset for name, _ in A.ArLayout._fields_}
+
+
 @pytest.mark.gpu
 def test_c_program_reduces_on_the_gpu(tmp_path):
     if not torch.cuda.is_available():
