@@ -185,17 +185,31 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
             for (; i + (E - 1) * stride < p.ne0; i += E * stride) {
                 float acc[E];
                 for (int r0 = 0; r0 < p.R; r0 += 4) {
+                    // the batch's row pointers first (NULL for an absent or
+                    // inactive rank, whose operand is +0), then all its loads,
+                    // then the wire rounding and the adds in rank order
+                    const char *rb[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = r0 + j;
+                        rb[j] = (r < p.R && !((p.inactive >> r) & 1u))
+                                    ? static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r]
+                                    : nullptr;
+                    }
                     float v[4][E];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
 #pragma unroll
                         for (int e = 0; e < E; ++e)
-                            v[j][e] = r0 + j < p.R ? ex_operand<Td, Tw>(p, r0 + j, row, i + e * stride) : 0.0f;
+                            v[j][e] = rb[j] ? load_elem<Td, false>(rb[j], static_cast<long long>(i + e * stride)) : 0.0f;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         if (r0 + j < p.R) {
 #pragma unroll
-                            for (int e = 0; e < E; ++e) acc[e] = (r0 + j == 0) ? v[j][e] : __fadd_rn(acc[e], v[j][e]);
+                            for (int e = 0; e < E; ++e) {
+                                const float x = wire1<Td, Tw>(v[j][e]);
+                                acc[e] = (r0 + j == 0) ? x : __fadd_rn(acc[e], x);
+                            }
                         }
                 }
                 if constexpr (RES) {
