@@ -24,25 +24,36 @@ struct ArExParams {
     int prefetch_ctas;                // CTAs (in launch order) that prefetch before the wait
 };
 
-// Operand r of element i of row `row`, rounded through the wire type; +0
-// for an inactive rank (the reduction of a zeroed partial).
-template <int Td, int Tw>
-__device__ __forceinline__ float ex_operand(const ArExParams &p, int r, size_t row, size_t i) {
-    if ((p.inactive >> r) & 1u) return 0.0f;
-    const char *base = static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
-    return wire1<Td, Tw>(load_elem<Td, false>(base, i));
-}
-
-// One element of a row, rank after rank (row tails and unaligned layouts;
-// kept sequential so the vector path's register budget is not raised).
+// One element of a row (row heads and tails, and the element-wise loop's
+// last elements): the loads of four ranks at a time are issued before any of
+// them is rounded and added (a load whose result is used before the next is
+// issued would leave one memory latency per rank on this thread).
 template <int Td, int Tw, bool RES>
 __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, size_t i) {
-    float acc = ex_operand<Td, Tw>(p, 0, row, i);
-    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, ex_operand<Td, Tw>(p, r, row, i));
+    float resv = 0.0f;
     if constexpr (RES) {
         const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
-        acc = __fadd_rn(acc, load_elem<Td, false>(rb, i));
+        resv = load_elem<Td, false>(rb, static_cast<long long>(i));
     }
+    float acc = 0.0f;
+    for (int r0 = 0; r0 < p.R; r0 += 4) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = r0 + j;
+            const char *b = (r < p.R && !((p.inactive >> r) & 1u))
+                                ? static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r]
+                                : nullptr;
+            v[j] = b ? load_elem<Td, false>(b, static_cast<long long>(i)) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < p.R) {
+                const float x = wire1<Td, Tw>(v[j]);
+                acc = (r0 + j == 0) ? x : __fadd_rn(acc, x);
+            }
+    }
+    if constexpr (RES) acc = __fadd_rn(acc, resv);
     for (int d = 0; d < p.n_dsts; ++d)
         store_elem<Td>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d], i, acc);
 }
