@@ -24,10 +24,36 @@ struct ArExParams {
     int prefetch_ctas;                // CTAs (in launch order) that prefetch before the wait
 };
 
-// One element of a row (row heads and tails, and the element-wise loop's
-// last elements): the loads of four ranks at a time are issued before any of
-// them is rounded and added (a load whose result is used before the next is
-// issued would leave one memory latency per rank on this thread).
+// Operand r of element i of row `row`, rounded through the wire type; +0
+// for an inactive rank (the reduction of a zeroed partial).
+template <int Td, int Tw>
+__device__ __forceinline__ float ex_operand(const ArExParams &p, int r, size_t row, size_t i) {
+    if ((p.inactive >> r) & 1u) return 0.0f;
+    const char *base = static_cast<const char *>(p.src[r]) + static_cast<long long>(row) * p.src_stride[r];
+    return wire1<Td, Tw>(load_elem<Td, false>(base, i));
+}
+
+// One element of a row, rank after rank: the row heads and tails of the
+// vector path.  Kept sequential, which keeps that kernel at the register
+// count it runs fastest with (the batched form below cut it from 48 to 40
+// registers per thread, and the extra resident CTAs made aligned layouts
+// 1.5% slower).
+template <int Td, int Tw, bool RES>
+__device__ __forceinline__ void ex_reduce_elem_seq(const ArExParams &p, size_t row, size_t i) {
+    float acc = ex_operand<Td, Tw>(p, 0, row, i);
+    for (int r = 1; r < p.R; ++r) acc = __fadd_rn(acc, ex_operand<Td, Tw>(p, r, row, i));
+    if constexpr (RES) {
+        const char *rb = static_cast<const char *>(p.residual) + static_cast<long long>(row) * p.res_stride;
+        acc = __fadd_rn(acc, load_elem<Td, false>(rb, i));
+    }
+    for (int d = 0; d < p.n_dsts; ++d)
+        store_elem<Td>(static_cast<char *>(p.dst[d]) + static_cast<long long>(row) * p.dst_stride[d], i, acc);
+}
+
+// One element of a row (the element-wise loop's last elements): the loads of
+// four ranks at a time are issued before any of them is rounded and added (a
+// load whose result is used before the next is issued would leave one memory
+// latency per rank on this thread).
 template <int Td, int Tw, bool RES>
 __device__ __forceinline__ void ex_reduce_elem(const ArExParams &p, size_t row, size_t i) {
     float resv = 0.0f;
@@ -186,7 +212,7 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
             // the threads after the last vector take the head's elements,
             // then the tail's
             const size_t u = v - vpr;
-            if (v >= vpr && u < h + t) ex_reduce_elem<Td, Tw, RES>(p, row, u < h ? u : u + vpr * V);
+            if (v >= vpr && u < h + t) ex_reduce_elem_seq<Td, Tw, RES>(p, row, u < h ? u : u + vpr * V);
         } else {
             // E elements a grid stride apart per thread, their loads for four
             // ranks at a time in flight before the fold
