@@ -940,8 +940,10 @@ int ar_reduce_ex(const void *const *srcs, void *const *dsts, int n_dsts, const a
     }
     if (gx < 1) gx = 1;
     const unsigned gy = L->ne1 < 65535 ? static_cast<unsigned>(L->ne1) : 65535u;
-    // the first wave prefetches its first row's operands into L2 before the wait
-    if (c.l2_prefetch) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
+    // the first wave of the vector kernel prefetches its first row's operands
+    // into L2 before the wait (in the element-wise kernel, measured, it did
+    // not help: R=2 unchanged, R=8 2.7% slower)
+    if (c.l2_prefetch && vec) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
     if (launch_dependent(fn, dim3(static_cast<unsigned>(gx), gy), static_cast<unsigned>(threads), 0, stream, c.pdl != 0,
                          p) != cudaSuccess) {
         cudaGetLastError();

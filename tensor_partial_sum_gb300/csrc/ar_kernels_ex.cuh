@@ -103,29 +103,6 @@ __global__ void __launch_bounds__(256) ar_reduce_ex_kernel(const __grid_constant
     constexpr int NW = VB / 4;
     constexpr int V = VB / Elem<Td>::bytes;
     pdl_launch_dependents();
-    if constexpr (!VEC) {
-        // the first wave asks L2 for its first row's first elements (as in
-        // ar_reduce_kernel's prefetch_first_round)
-        const size_t cta = static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-        const size_t row = blockIdx.y;
-        if (cta < static_cast<size_t>(p.prefetch_ctas) && row < p.ne1) {
-            const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-            const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-            for (int e = 0; e < 4; ++e) {
-                const size_t i = i0 + e * stride;
-                if (i >= p.ne0) break;
-                for (int r = 0; r < p.R; ++r)
-                    if (!((p.inactive >> r) & 1u))
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.src[r]) +
-                                                                      static_cast<long long>(row) * p.src_stride[r] +
-                                                                      i * Elem<Td>::bytes));
-                if constexpr (RES)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p.residual) +
-                                                                  static_cast<long long>(row) * p.res_stride +
-                                                                  i * Elem<Td>::bytes));
-            }
-        }
-    }
     if constexpr (VEC) {
         // the first wave asks L2 for its first row's operands (as in
         // ar_reduce_kernel's prefetch_first_round)
