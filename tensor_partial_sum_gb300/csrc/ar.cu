@@ -431,9 +431,10 @@ int launch_locked(const void *const *srcs, void *const *dsts, int n_dsts, size_t
         if (c.l2_prefetch && device_buffers) p.prefetch_ctas = first_wave(fn, threads, c.sm_count);
     }
     // The kernels wait (griddepcontrol.wait) for the kernel before them on
-    // the stream before touching memory, so they may be launched as
-    // programmatic dependents: the launch then overlaps that kernel's last
-    // wave.  The naive cross-check kernel has no such wait and launches plainly.
+    // the stream before they load or store anything (their first wave only
+    // prefetches into L2 before it), so they may be launched as programmatic
+    // dependents: the launch then overlaps that kernel's last wave.  The
+    // naive cross-check kernel has no such wait and launches plainly.
     if (launch_dependent(fn, dim3(static_cast<unsigned>(grid)), static_cast<unsigned>(threads), 0, stream,
                          c.pdl != 0 && variant != AR_VARIANT_NAIVE, p) != cudaSuccess) {
         cudaGetLastError();
