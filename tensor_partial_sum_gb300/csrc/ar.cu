@@ -219,8 +219,8 @@ const char *variant_name(int v) {
 }
 
 // Launch a kernel that runs griddepcontrol.launch_dependents and
-// griddepcontrol.wait before touching memory: as a programmatic dependent of
-// the kernel before it on the stream when `pdl`, else plainly.
+// griddepcontrol.wait before it loads or stores anything: as a programmatic
+// dependent of the kernel before it on the stream when `pdl`, else plainly.
 template <typename... Params, typename... Args>
 cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, unsigned threads, size_t smem, cudaStream_t stream,
                              bool pdl, Args... args) {
