@@ -834,6 +834,29 @@ def test_chained_reductions_see_the_previous_results(ctx, prefetch, n, monkeypat
         assert_same(to_host(outs[k], "f32"), exp[k], "f32", f"step {k + 1} AR_L2_PREFETCH={prefetch}")
 
 
+@pytest.mark.parametrize("prefetch", ["0", "1"])
+def test_prefetch_on_and_off_give_the_same_bits_for_every_variant(ctx, prefetch, monkeypatch):
+    """AR_L2_PREFETCH=0 turns the first wave's L2 prefetch off; every variant
+    gives the oracle's bits either way, two launches back to back on a
+    created stream (the second a programmatic dependent of the first)."""
+    monkeypatch.setenv("AR_L2_PREFETCH", prefetch)
+    tps.ar_init(3, 1 << 20)
+    ctx.R = None  # the next test re-initialises with its own limits (and without the variable)
+    n = 300_007
+    srcs = srcs_for(4343, 3, n, "bf16")
+    exp = expect(srcs, "bf16", "f16")
+    stream = torch.cuda.Stream()
+    for v in VARIANTS:
+        d_srcs = [to_device(s, "bf16") for s in srcs]
+        d_dsts = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        torch.cuda.synchronize()
+        for _ in range(2):
+            tps.ar_reduce_variant(d_srcs, d_dsts, v, dst_dtype="bf16", wire_dtype="f16", stream=stream)
+        torch.cuda.synchronize()
+        for d in d_dsts:
+            assert_same(to_host(d, "bf16"), exp, "bf16", f"AR_L2_PREFETCH={prefetch} variant={v}")
+
+
 @pytest.mark.parametrize("variant", ["auto", "latency", "bandwidth", "scalar"])
 def test_prepared_call_gives_the_same_bits(ctx, variant):
     n = 50_003
